@@ -1,0 +1,151 @@
+/*
+ * pa.h -- paged-attention decode on GB300 (sm_103a): the C ABI of libpa103.so.
+ *
+ * The operation.  A decode step gives each sequence b a few new query tokens
+ * (q_lens[b] <= max_q_len rows per query head) that attend over that
+ * sequence's cached keys and values.  The cache is a pool of fixed-size
+ * physical pages; sequence b reaches its logical page p at physical block
+ * block_tables[b][p] ("HSTU Paged Attention", RecSDK issue 1281, background:
+ * historical K/V are read page by page from the paged KV cache).  For query
+ * head h (KV head g = h / (Hq / Hkv)) and new-token row i < q_lens[b]:
+ *
+ *     n   = context_lens[b]          (counts the q_lens[b] new tokens, which are
+ *                                     the last q_lens[b] positions)
+ *     L   = causal ? n - q_lens[b] + i + 1 : n     visible keys 0 .. L-1
+ *     s_j = sm_scale * <q[b,i,h,:], k_j>           k_j = K[block_tables[b][j/bs], j%bs, g, :]
+ *     out[b,i,h,:] = sum_j softmax(s)_j v_j ,  lse[b,i,h] = log sum_j exp(s_j)
+ *
+ * Rows i >= q_lens[b] are padding: out = 0, lse = -inf.
+ *
+ * The work is split as in "Optimize paged-attention metadata decode" (FlyDSL
+ * PR #910, Summary and Changes): a planner emits a work list for a persistent
+ * grid of one CTA per SM (times a grid multiplier, default 1); a persistent
+ * decode kernel processes it, writing whole results directly and per-range
+ * partials (o_s, lse_s) otherwise; a reducer merges the partials by
+ *     m* = max_s lse_s,  w_s = exp(lse_s - m*),  out = sum_s w_s o_s / sum_s w_s.
+ * fp8 caches hold OCP E4M3 codes with one fp32 scale per tensor or one per
+ * (block, slot, kv-head) row (FlyDSL PR #910, per_token_kv scale mode).
+ *
+ * Calling convention.  The caller owns all memory.  pa_plan, pa_decode and
+ * pa_reduce allocate nothing, never synchronise the host and never abort: each
+ * validates its arguments on the host, enqueues its kernel on `stream` and
+ * returns a status.  They are stream-ordered, so the three calls on one stream
+ * with one workspace form one decode step and can be captured in a CUDA graph.
+ * Problems in the device-resident lengths or block tables cannot be seen by the
+ * host; the planner records them as flags in the workspace and empties the
+ * work list so no kernel touches memory outside the inputs.  pa_read_flags
+ * (the one synchronising call) returns them.
+ *
+ * Device pointers: q, k_cache, v_cache, k_scale, v_scale, block_tables,
+ * context_lens, q_lens, out, lse and ws.  q, k_cache, v_cache and out must be
+ * 16-byte aligned; ws 256-byte aligned.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entry points are the only symbols the library exports. */
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+/* The same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *pa_stream;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null pointer, misalignment, negative size, bad enum value */
+  PA_ERR_UNSUPPORTED = 2, /* head_dim, block_size or dtype combination not supported */
+  PA_ERR_WORKSPACE = 3,   /* ws_bytes below pa_workspace_size() */
+  PA_ERR_CUDA = 4,        /* a CUDA runtime call or a kernel launch failed */
+  PA_ERR_DEVICE = 5       /* pa_read_flags: the device recorded an input problem */
+} pa_status;
+
+typedef enum { PA_BF16 = 0, PA_FP16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
+
+typedef enum {
+  PA_SCALE_NONE = 0,       /* 16-bit cache, or fp8 codes used as they are */
+  PA_SCALE_PER_TENSOR = 1, /* k_scale, v_scale: one fp32 each */
+  PA_SCALE_PER_TOKEN = 2   /* k_scale, v_scale: fp32 [num_blocks, block_size, num_kv_heads] */
+} pa_scale_mode;
+
+/* Device-side input problems, OR-ed into the flags word. */
+enum {
+  PA_FLAG_BAD_LENGTHS = 1,   /* q_lens[b] outside [0, max_q_len], context_lens[b] < q_lens[b],
+                                or context_lens[b] > max_blocks_per_seq * block_size */
+  PA_FLAG_BAD_BLOCK_ID = 2,  /* a block_tables entry in use lies outside [0, num_blocks) */
+  PA_FLAG_WAIT_TIMEOUT = 4   /* a kernel gave up a bounded wait on its own copies */
+};
+
+typedef struct {
+  int32_t batch;              /* B >= 1 */
+  int32_t max_q_len;          /* Sq >= 1: query rows per sequence in q and out */
+  int32_t num_q_heads;        /* Hq */
+  int32_t num_kv_heads;       /* Hkv, divides Hq */
+  int32_t head_dim;           /* D: 64, 128 or 256 */
+  int32_t block_size;         /* tokens per page: a power of two in [16, 1024] */
+  int32_t max_blocks_per_seq; /* columns of block_tables */
+  int32_t num_blocks;         /* physical pages in the pool */
+  int32_t q_dtype;            /* pa_dtype of q and out: PA_BF16 or PA_FP16 */
+  int32_t kv_dtype;           /* pa_dtype of the cache: q_dtype or PA_FP8_E4M3 */
+  int32_t kv_scale_mode;      /* pa_scale_mode; PA_SCALE_NONE unless kv_dtype is fp8 */
+  int32_t causal;             /* 1: new token i sees keys up to its own position */
+  float sm_scale;             /* logit scale, usually 1/sqrt(D) */
+  int32_t num_ctas;           /* persistent grid size; 0: SMs of the current device x grid_mult */
+  int32_t grid_mult;          /* CTAs per SM when num_ctas is 0; 0 means 1 */
+} pa_config;
+
+/* Bytes of workspace a pa_plan/pa_decode/pa_reduce sequence needs for cfg:
+ * the work list for (C + units) items and fp32 partials for as many splits,
+ * where C is the persistent grid size and units = B * Hkv * row blocks.
+ * May query the current device (num_ctas == 0).  Writes *bytes. */
+PA_API pa_status pa_workspace_size(const pa_config *cfg, size_t *bytes);
+
+/* Plan one decode step (device work, no host sync).  Reads context_lens[B],
+ * q_lens[B] and block_tables[B][max_blocks_per_seq] (int32, row-major); checks
+ * the lengths and every block id in use; writes the work list into ws.  Cuts the
+ * concatenated token ranges of all (sequence, kv-head, row-block) units into C
+ * contiguous tile-aligned pieces of equal size, one per CTA, so every CTA of the
+ * persistent grid reads the same number of pages. */
+PA_API pa_status pa_plan(const pa_config *cfg, const int32_t *block_tables, const int32_t *context_lens,
+                  const int32_t *q_lens, void *ws, size_t ws_bytes, pa_stream stream);
+
+/* Run the persistent decode over the work list pa_plan left in ws.
+ *   q        [B, Sq, Hq, D]            q_dtype
+ *   k_cache  [num_blocks, block_size, Hkv, D]   kv_dtype (uint8 codes for fp8)
+ *   v_cache  same layout as k_cache
+ *   k_scale, v_scale  NULL unless fp8 with a scale mode (see pa_scale_mode)
+ *   out      [B, Sq, Hq, D]            q_dtype; written for units done in one piece
+ *   lse      [B, Sq, Hq] fp32 natural-log LSE, or NULL
+ * The tables and lengths must be the ones given to pa_plan. */
+PA_API pa_status pa_decode(const pa_config *cfg, const void *q, const void *k_cache, const void *v_cache,
+                    const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                    const int32_t *context_lens, const int32_t *q_lens, void *out, float *lse,
+                    void *ws, size_t ws_bytes, pa_stream stream);
+
+/* Merge the split partials of every unit pa_decode left in ws into out (and lse),
+ * and write the padding rows of units with no keys.  Completes the step. */
+PA_API pa_status pa_reduce(const pa_config *cfg, void *out, float *lse, void *ws, size_t ws_bytes,
+                    pa_stream stream);
+
+/* Synchronise `stream` and return the device flags of the last plan/decode in ws
+ * (PA_FLAG_* bits; 0 when the step was clean) in *flags.  Returns PA_ERR_DEVICE
+ * when any flag is set, PA_OK otherwise. */
+PA_API pa_status pa_read_flags(const void *ws, size_t ws_bytes, int32_t *flags, pa_stream stream);
+
+/* A static, human-readable name of a status. */
+PA_API const char *pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,12 @@
+// CUDA-core decode kernel instances for head dim 64 (one translation unit per head dim
+// so the instances compile in parallel).
+#include "decode_simt.cuh"
+
+namespace pa {
+
+cudaError_t launch_simt_d64(const SimtParams& prm, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           int grid, int mp, int kvk, int qk, bool toks, cudaStream_t s) {
+  return launch_simt_for_dim<64>(prm, kmap, vmap, grid, mp, kvk, qk, toks, s);
+}
+
+}  // namespace pa

@@ -1,0 +1,259 @@
+// Internal definitions shared by the planner, decode and reduce kernels and the C ABI:
+// the kernel variant chosen for a configuration, the workspace layout, and thin
+// wrappers over the sm_100-family PTX used for staging (mbarrier, TMA, cp.async).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned kFull = 0xffffffffu;
+
+enum KvKind { KV_BF16 = 0, KV_FP16 = 1, KV_FP8 = 2 };
+enum QKind { Q_BF16 = 0, Q_FP16 = 1 };
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr int round_up(int a, int b) { return ceil_div(a, b) * b; }
+__host__ __device__ constexpr size_t round_up_sz(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+// ---------------------------------------------------------------------------------
+// Kernel variant.  M = G * Sq query rows share one kv head.  Rows are processed in
+// tiles of `mp` (a power of two); a unit of work is one (sequence, kv head, row
+// tile), and `tt` is the number of tokens staged per pipeline stage.
+struct Variant {
+  int rows;    // M = G * Sq
+  int mp;      // rows per unit (padded to a power of two)
+  int rb;      // row tiles per kv head
+  int tt;      // tokens per stage (tile)
+  int units;   // B * Hkv * rb
+  int ctas;    // persistent grid size C
+  int bpe;     // bytes per cache element
+};
+
+// Largest row tile of the CUDA-core decode kernel.
+constexpr int kSimtMaxRows = 8;
+// Bytes of one K (or V) tile of a stage.
+constexpr int kTileBytes = 16384;
+
+inline int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+inline Variant make_variant(const pa_config& c, int ctas) {
+  Variant v{};
+  v.rows = (c.num_q_heads / c.num_kv_heads) * c.max_q_len;
+  v.mp = v.rows <= kSimtMaxRows ? pow2_at_least(v.rows) : kSimtMaxRows;
+  v.rb = ceil_div(v.rows, v.mp);
+  v.bpe = c.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
+  v.tt = kTileBytes / (c.head_dim * v.bpe);
+  v.units = c.batch * c.num_kv_heads * v.rb;
+  v.ctas = ctas;
+  return v;
+}
+
+// ---------------------------------------------------------------------------------
+// Workspace layout (byte offsets from ws, every section 256-byte aligned).
+//   header     int32[64]: [0] flags, [1] chunk, [2] active CTAs, [3] items
+//   item_off   int32[C + 1]      first work item of each CTA
+//   items      int4[C + units]   (unit, t0, t1, partial slot or -1)
+//   unit_info  int2[units]       (first partial slot, number of splits)
+//   unit_start int32[units + 1]  start of each unit in the concatenated token space
+//   o_part     f32[(C + units) * mp * D]   normalised partial outputs
+//   lse_part   f32[(C + units) * mp]       their log2-sum-exp
+struct WsLayout {
+  size_t header, item_off, items, unit_info, unit_start, o_part, lse_part, total;
+};
+
+inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = round_up_sz(off + bytes, 256);
+    return at;
+  };
+  const size_t max_items = (size_t)v.ctas + (size_t)v.units;
+  L.header = take(64 * sizeof(int32_t));
+  L.item_off = take(((size_t)v.ctas + 1) * sizeof(int32_t));
+  L.items = take(max_items * sizeof(int4));
+  L.unit_info = take((size_t)v.units * sizeof(int2));
+  L.unit_start = take(((size_t)v.units + 1) * sizeof(int32_t));
+  L.o_part = take(max_items * (size_t)v.mp * c.head_dim * sizeof(float));
+  L.lse_part = take(max_items * (size_t)v.mp * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+enum HeaderSlot { HDR_FLAGS = 0, HDR_CHUNK = 1, HDR_ACTIVE = 2, HDR_ITEMS = 3 };
+
+// Launch helpers implemented in plan.cu / decode_*.cu / reduce.cu.
+struct ProblemArgs {
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* q_lens;
+  int batch, max_q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks;
+  int causal;
+};
+
+cudaError_t launch_plan(const ProblemArgs& a, const Variant& v, const WsLayout& L, char* ws,
+                        cudaStream_t s);
+
+struct DecodeArgs {
+  ProblemArgs p;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  int scale_mode;
+  float qk_scale;  // sm_scale * log2(e)
+  void* out;
+  float* lse;
+  char* ws;
+  WsLayout L;
+  Variant v;
+  int q_kind, kv_kind;
+};
+
+// Returns cudaErrorNotSupported when no kernel instance matches.
+cudaError_t launch_decode_simt(const DecodeArgs& a, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t s);
+
+cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------
+// Device helpers.
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Longest a kernel waits for one of its own copies before it gives up.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Bounded wait on phase `parity`.  Returns false when the wait ran out or another warp of
+// the CTA has already given up (*abort != 0); the caller then records the failure and
+// stops waiting, so the kernel always ends.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (*abort) return false;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used at exit, to let copies already in
+// flight land before the CTA's shared memory is released.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 4-D tiled TMA load of one box into shared memory, completing on `bar` (tx bytes).
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Named barrier over the first `count` threads of the CTA (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+#endif  // __CUDACC__
+
+}  // namespace pa

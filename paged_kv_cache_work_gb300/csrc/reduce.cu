@@ -1,0 +1,137 @@
+// Split reducer and the decode dispatch.
+//
+// The reducer merges, for every unit the planner cut into several pieces, the normalised
+// partials o_s and their log2-sum-exp l_s:  m* = max_s l_s,  w_s = 2^(l_s - m*),
+// out = sum_s w_s o_s / sum_s w_s,  lse = (m* + log2 sum_s w_s) ln 2.  This is the "split
+// reducer" that follows the persistent decode in "Optimize paged-attention metadata
+// decode" (FlyDSL PR #910, Summary and Performance: metadata decode plus split reducer).
+// Units the decode finished in one piece are skipped; units with no keys at all (a
+// sequence with no context) get zero rows and lse = -inf.  The sum over splits runs in a
+// fixed order, so repeated calls are bitwise identical.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "decode_simt.cuh"
+
+namespace pa {
+
+cudaError_t launch_simt_d64(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+                            int, int, bool, cudaStream_t);
+cudaError_t launch_simt_d128(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+                             int, int, bool, cudaStream_t);
+cudaError_t launch_simt_d256(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+                             int, int, bool, cudaStream_t);
+
+SimtParams make_simt_params(const DecodeArgs& a) {
+  SimtParams p{};
+  p.q = a.q;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.bt = a.p.block_tables;
+  p.ctx = a.p.context_lens;
+  p.qlens = a.p.q_lens;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.item_off = reinterpret_cast<const int32_t*>(a.ws + a.L.item_off);
+  p.items = reinterpret_cast<const int4*>(a.ws + a.L.items);
+  p.o_part = reinterpret_cast<float*>(a.ws + a.L.o_part);
+  p.lse_part = reinterpret_cast<float*>(a.ws + a.L.lse_part);
+  p.flags = reinterpret_cast<int32_t*>(a.ws + a.L.header) + HDR_FLAGS;
+  p.scale_mode = a.scale_mode;
+  p.Sq = a.p.max_q_len;
+  p.Hq = a.p.num_q_heads;
+  p.Hkv = a.p.num_kv_heads;
+  p.G = a.p.num_q_heads / a.p.num_kv_heads;
+  p.M = a.v.rows;
+  p.RB = a.v.rb;
+  p.bs = a.p.block_size;
+  p.maxb = a.p.max_blocks;
+  p.nblocks = a.p.num_blocks;
+  p.causal = a.p.causal;
+  p.qk_scale = a.qk_scale;
+  return p;
+}
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t s) {
+  const SimtParams prm = make_simt_params(a);
+  const bool toks = a.scale_mode == PA_SCALE_PER_TOKEN;
+  switch (a.p.head_dim) {
+    case 64: return launch_simt_d64(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+    case 128: return launch_simt_d128(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+    case 256: return launch_simt_d256(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+namespace {
+
+struct ReduceParams {
+  void* out;
+  float* lse;
+  const int2* unit_info;
+  const float* o_part;
+  const float* lse_part;
+  int Sq, Hq, Hkv, G, M, RB, MP, D;
+  int q_kind;
+};
+
+__global__ void __launch_bounds__(256) reduce_kernel(const ReduceParams p) {
+  const int u = blockIdx.x;
+  const int2 info = p.unit_info[u];
+  if (info.y == 1) return;  // written by the decode kernel
+  const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
+  for (int e = threadIdx.x; e < p.MP * p.D; e += blockDim.x) {
+    const int r = e / p.D, d = e % p.D, rg = rb * p.MP + r;
+    if (rg >= p.M) continue;
+    float val = 0.f, lse2 = -INFINITY;
+    if (info.y >= 2) {
+      float m = -INFINITY;
+      for (int s = 0; s < info.y; ++s) m = fmaxf(m, p.lse_part[(size_t)(info.x + s) * p.MP + r]);
+      if (m != -INFINITY) {
+        float W = 0.f, O = 0.f;
+        for (int s = 0; s < info.y; ++s) {
+          const size_t part = (size_t)(info.x + s) * p.MP + r;
+          const float ls = p.lse_part[part];
+          const float w = ls == -INFINITY ? 0.f : fast_exp2(ls - m);
+          W += w;
+          O += w * p.o_part[part * p.D + d];
+        }
+        val = O / W;
+        lse2 = m + fast_log2(W);
+      }
+    }
+    const int i = rg / p.G, h = g * p.G + rg % p.G;
+    const size_t row = ((size_t)b * p.Sq + i) * p.Hq + h;
+    if (p.q_kind == Q_BF16)
+      reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.D + d] = __float2bfloat16_rn(val);
+    else
+      reinterpret_cast<__half*>(p.out)[row * p.D + d] = __float2half_rn(val);
+    if (d == 0 && p.lse) p.lse[row] = lse2 * kLn2;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s) {
+  ReduceParams p;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.unit_info = reinterpret_cast<const int2*>(a.ws + a.L.unit_info);
+  p.o_part = reinterpret_cast<const float*>(a.ws + a.L.o_part);
+  p.lse_part = reinterpret_cast<const float*>(a.ws + a.L.lse_part);
+  p.Sq = a.p.max_q_len;
+  p.Hq = a.p.num_q_heads;
+  p.Hkv = a.p.num_kv_heads;
+  p.G = a.p.num_q_heads / a.p.num_kv_heads;
+  p.M = a.v.rows;
+  p.RB = a.v.rb;
+  p.MP = a.v.mp;
+  p.D = a.p.head_dim;
+  p.q_kind = a.q_kind;
+  if (a.v.units == 0) return cudaSuccess;
+  reduce_kernel<<<a.v.units, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,144 @@
+"""The planner's work list, read back from the workspace (GPU).
+
+* bit-exact coverage: every (sequence, kv head, row tile, token) lies in exactly one work
+  item, and items never reach past a sequence's context;
+* every CTA's piece is contiguous in the concatenated tile-padded token space and no
+  longer than the chunk, and the chunk is the smallest tile multiple that fits the work
+  in C pieces;
+* the partial slots of units cut into several pieces are distinct and dense;
+* each partial the decode kernel wrote equals the oracle's attention over that item's
+  key range (so the split mode is checked on its own, before the reducer).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_run import plan_view, run
+from pagedkv import random_problem
+
+pytestmark = pytest.mark.gpu
+
+
+def check_plan(view, ctx, ctas, hkv):
+    """Exact checks of the work list against the cutting rule stated in pa.h."""
+    v = view["v"]
+    tt, U, rb = v["tt"], v["units"], v["rb"]
+    per_seq = hkv * rb
+    lens = np.array([ctx[u // per_seq] for u in range(U)], np.int64)
+    plen = -(-lens // tt) * tt
+    start = np.concatenate([[0], np.cumsum(plen)])
+    T = int(start[-1])
+    chunk = view["chunk"]
+    if T > 0:
+        assert chunk == -(-(-(-T // ctas)) // tt) * tt
+        assert view["active"] == -(-T // chunk) <= ctas
+    else:
+        assert view["active"] == 0
+    item_off, items = view["item_off"], view["items"]
+    assert item_off[0] == 0 and (np.diff(item_off) >= 0).all()
+    assert item_off[-1] == view["n_items"]
+    covered = [np.zeros(int(n), np.int32) for n in lens]
+    slots = {}
+    for c in range(ctas):
+        active = c < view["active"]
+        lo = c * chunk
+        hi = min(lo + chunk, T) if active else lo
+        pos = lo
+        for it in range(item_off[c], item_off[c + 1]):
+            u, t0, t1, slot = (int(x) for x in items[it])
+            assert active and 0 <= u < U
+            if t1 <= t0:
+                assert lens[u] == 0
+                continue
+            assert 0 <= t0 < t1 <= lens[u] and t0 % tt == 0
+            assert start[u] + t0 == pos, "piece not contiguous"
+            if t1 < lens[u]:
+                assert t1 % tt == 0
+                pos = start[u] + t1
+            else:
+                pos = start[u] + plen[u]
+            covered[u][t0:t1] += 1
+            slots.setdefault(u, []).append(slot)
+        assert pos == hi, "piece does not end where the next begins"
+    for u in range(U):
+        assert (covered[u] == 1).all(), f"unit {u} not covered exactly once"
+        info = view["unit_info"][u]
+        ns = len(slots.get(u, []))
+        assert int(info[1]) == ns
+        if ns == 1:
+            assert slots[u] == [-1]
+        elif ns > 1:
+            assert slots[u] == list(range(int(info[0]), int(info[0]) + ns))
+    return T
+
+
+CASES = [
+    ("gqa", W.reduced(W.GQA_B32, 7, 1, 3000), [152, 5, 1, 1000]),
+    ("long_sq4", W.reduced(W.LONG_SQ4, 3, 4, 20000), [152, 3]),
+    ("mha_sq16", W.reduced(W.mha_d256(8, 16), 3, 16, 4000), [152, 64]),
+    ("fp8_token", W.reduced(W.FP8_TOKEN_SQ1, 5, 1, 5000), [152, 9]),
+]
+
+
+@pytest.mark.parametrize("name,wl,grids", CASES, ids=[c[0] for c in CASES])
+def test_work_list_covers_every_token_once(name, wl, grids, cuda_device, pa):
+    for seed in W.SEEDS:
+        inp = W.make_inputs(wl, seed, device=cuda_device)
+        ctx = inp["context_lens"].cpu().numpy()
+        for ctas in grids:
+            _, _, ws, cfg = run(inp, num_ctas=ctas)
+            view = plan_view(ws, cfg, ctas)
+            assert view["flags"] == 0
+            check_plan(view, ctx, ctas, wl.num_kv_heads)
+
+
+def test_random_shapes_coverage(cuda_device, pa):
+    rng = np.random.default_rng(99)
+    for trial in range(12):
+        B = int(rng.integers(1, 9))
+        ctx = [int(x) for x in rng.integers(0, 700, size=B)]
+        ctx[0] = max(ctx[0], 1)
+        kw = dict(batch=B, max_q_len=1, num_q_heads=4, num_kv_heads=int(rng.choice([1, 2, 4])),
+                  head_dim=int(rng.choice([64, 128])), block_size=int(rng.choice([16, 32, 128])),
+                  ctx=ctx, q_lens=[min(1, n) for n in ctx])
+        inp, _ = random_problem(rng, **kw)
+        dev = W.to_device(inp, cuda_device)
+        for ctas in (1, 3, 152):
+            _, _, ws, cfg = run(dev, num_ctas=ctas)
+            check_plan(plan_view(ws, cfg, ctas), ctx, ctas, kw["num_kv_heads"])
+
+
+def test_partials_equal_oracle_ranges(cuda_device, pa):
+    wl = W.reduced(W.LONG_SQ4, 2, 3000, 7000)
+    inp = W.make_inputs(wl, 2026)
+    dev = W.to_device(inp, cuda_device)
+    ctas = 16
+    _, _, ws, cfg = run(dev, num_ctas=ctas)
+    view = plan_view(ws, cfg, ctas)
+    v = view["v"]
+    G = wl.num_q_heads // wl.num_kv_heads
+    checked = 0
+    for it in range(view["n_items"]):
+        u, t0, t1, slot = (int(x) for x in view["items"][it])
+        if slot < 0 or t1 <= t0:
+            continue
+        b = u // (wl.num_kv_heads * v["rb"])
+        g = (u // v["rb"]) % wl.num_kv_heads
+        rb = u % v["rb"]
+        for r in range(v["mp"]):
+            rg = rb * v["mp"] + r
+            if rg >= v["rows"]:
+                continue
+            i, h = rg // G, g * G + rg % G
+            o, lse = oracle.attend_range(inp, b, i, h, t0, t1, "f64")
+            got_o = view["o_part"][slot, r]
+            got_l = view["lse_part"][slot, r] * np.log(2.0)
+            if not np.isfinite(lse):
+                assert got_l == -np.inf and np.all(got_o == 0)
+                continue
+            assert np.abs(got_o - o).max() <= 2e-3 + 2e-3 * np.abs(o).max()
+            assert abs(got_l - lse) <= 2e-4 * (1 + abs(lse))
+            checked += 1
+    assert checked > 0
