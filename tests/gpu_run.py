@@ -125,6 +125,7 @@ def sample_rows(w: workloads.Workload, ql, n: int, seed: int):
     """n distinct (b, i, h) rows, always including the first and last valid rows."""
     rng = np.random.default_rng(seed)
     rows = {(0, 0, 0), (w.batch - 1, int(ql[-1]) - 1, w.num_q_heads - 1)}
+    n = min(n, int(sum(max(1, int(x)) for x in ql)) * w.num_q_heads)  # distinct rows that exist
     while len(rows) < n:
         b = int(rng.integers(w.batch))
         rows.add((b, int(rng.integers(max(1, int(ql[b])))), int(rng.integers(w.num_q_heads))))
