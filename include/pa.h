@@ -141,6 +141,35 @@ PA_API pa_status pa_reduce(const pa_config *cfg, void *out, float *lse, void *ws
  * when any flag is set, PA_OK otherwise. */
 PA_API pa_status pa_read_flags(const void *ws, size_t ws_bytes, int32_t *flags, pa_stream stream);
 
+/* Size of the device scratch array behind pa_decode_step_static (16 MiB). */
+#define PA_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* One whole decode step (plan, decode, reduce) that allocates nothing and needs no
+ * workspace from the caller.  The pages have no counterpart: it exists for callers that
+ * cannot allocate device memory -- code running under a framework or plugin interface that
+ * hands out no allocator, loops that must not call cudaMalloc once serving has started
+ * (cudaMalloc can synchronise the device and is not allowed during stream capture), and
+ * deployments that forbid allocation after start-up.  Arguments are those of pa_decode
+ * without ws/ws_bytes; the caller still provides q, the caches, scales, tables, lengths,
+ * out and lse.
+ *
+ * The scratch is one file-scope __device__ array of PA_STATIC_SCRATCH_BYTES, reserved on
+ * every GPU where the library's device code is loaded and held until the process exits.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current and caches it; make that first call before any stream capture.
+ * A problem whose pa_workspace_size() exceeds PA_STATIC_SCRATCH_BYTES is rejected with
+ * PA_ERR_WORKSPACE before anything is launched.  All calls on a device share the one array
+ * and each call overwrites what the previous one left there: calls whose kernels overlap on
+ * the GPU (different streams, or different host threads without ordering) race and corrupt
+ * each other's results.  Calls on one stream are ordered and safe.  pa_read_flags is not
+ * available for this scratch (its address is private); device-side input problems leave
+ * out unspecified. */
+PA_API pa_status pa_decode_step_static(const pa_config *cfg, const void *q, const void *k_cache,
+                                       const void *v_cache, const float *k_scale,
+                                       const float *v_scale, const int32_t *block_tables,
+                                       const int32_t *context_lens, const int32_t *q_lens,
+                                       void *out, float *lse, pa_stream stream);
+
 /* A static, human-readable name of a status. */
 PA_API const char *pa_status_string(pa_status status);
 

@@ -15,6 +15,7 @@ import os
 from typing import Optional
 
 __all__ = ["PaConfig", "PaError", "load", "workspace_size", "plan", "decode", "reduce",
+           "decode_step_static", "STATIC_SCRATCH_BYTES",
            "read_flags", "status_string", "config_for", "paged_attention", "LIB_PATH",
            "BF16", "FP16", "FP8_E4M3", "SCALE_NONE", "SCALE_PER_TENSOR", "SCALE_PER_TOKEN",
            "FLAG_BAD_LENGTHS", "FLAG_BAD_BLOCK_ID", "FLAG_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
@@ -30,7 +31,10 @@ SCALE_NONE, SCALE_PER_TENSOR, SCALE_PER_TOKEN = 0, 1, 2
 FLAG_BAD_LENGTHS, FLAG_BAD_BLOCK_ID, FLAG_WAIT_TIMEOUT = 1, 2, 4
 
 EXPORTED_SYMBOLS = ("pa_workspace_size", "pa_plan", "pa_decode", "pa_reduce", "pa_read_flags",
-                    "pa_status_string")
+                    "pa_status_string", "pa_decode_step_static")
+
+# Bytes of the device array behind pa_decode_step_static (PA_STATIC_SCRATCH_BYTES).
+STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class PaConfig(ctypes.Structure):
@@ -67,6 +71,8 @@ def load(path: str = LIB_PATH):
     L.pa_read_flags.argtypes = [vp, sz, ctypes.POINTER(ctypes.c_int32), vp]
     for f in ("pa_workspace_size", "pa_plan", "pa_decode", "pa_reduce", "pa_read_flags"):
         getattr(L, f).restype = ctypes.c_int
+    L.pa_decode_step_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.pa_decode_step_static.restype = ctypes.c_int
     L.pa_status_string.argtypes = [ctypes.c_int]
     L.pa_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -134,6 +140,16 @@ def read_flags(ws, stream=None) -> int:
     if st not in (OK, ERR_DEVICE):
         raise PaError("pa_read_flags", st)
     return f.value
+
+
+def decode_step_static(cfg: PaConfig, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                       context_lens, q_lens, out, lse, stream=None):
+    """One decode step on the library's static device scratch, for callers that cannot
+    allocate device memory (no workspace argument; see pa_decode_step_static in pa.h)."""
+    _check("pa_decode_step_static", load().pa_decode_step_static(
+        ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_tables), _ptr(context_lens), _ptr(q_lens), _ptr(out), _ptr(lse),
+        _stream(stream)))
 
 
 _DT = {"bf16": BF16, "fp16": FP16, "fp8": FP8_E4M3}
