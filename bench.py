@@ -372,7 +372,7 @@ def run_ours(args, rank, world, local):
                 "l2": (f"inputs larger than L2: 2 input sets of {int(bytes_per_launch) >> 20} MiB KV "
                        f"alternate (L2 {l2 >> 20} MiB)"),
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                "grid": int(sets[0]["cfg"].num_ctas) or props.multi_processor_count,
+                "split_merge": "in decode (last CTA of a unit merges)",
             },
             "roofline": {
                 "kernel": DECODE_KERNEL, "bound": "hbm", "achieved": round(achieved_gbs, 1),

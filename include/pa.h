@@ -32,9 +32,11 @@
  * returns a status.  They are stream-ordered, so the three calls on one stream
  * with one workspace form one decode step and can be captured in a CUDA graph.
  * Problems in the device-resident lengths or block tables cannot be seen by the
- * host; the planner records them as flags in the workspace and empties the
- * work list so no kernel touches memory outside the inputs.  pa_read_flags
- * (the one synchronising call) returns them.
+ * host.  The planner flags bad lengths and empties the work list (the output is
+ * then all zeros with lse = -inf); the decode kernel checks every block id before
+ * it loads the page, skips a page outside the pool and flags it (the rows of that
+ * sequence are then unspecified).  Either way no kernel touches memory outside the
+ * inputs.  pa_read_flags (the one synchronising call) returns the flags.
  *
  * Device pointers: q, k_cache, v_cache, k_scale, v_scale, block_tables,
  * context_lens, q_lens, out, lse and ws.  q, k_cache, v_cache and out must be
@@ -77,6 +79,13 @@ typedef enum {
   PA_SCALE_PER_TOKEN = 2   /* k_scale, v_scale: fp32 [num_blocks, block_size, num_kv_heads] */
 } pa_scale_mode;
 
+/* Where the log-sum-exp merge of split units runs.  PA_MERGE_IN_DECODE (the default, 0):
+ * the last CTA to finish a piece of a unit merges that unit's partials inside pa_decode
+ * (an atomic arrival counter per unit; no CTA ever waits for another), so pa_decode leaves
+ * the finished output and pa_reduce launches nothing.  PA_MERGE_IN_REDUCE: pa_decode only
+ * writes the partials and pa_reduce merges them in its own kernel. */
+typedef enum { PA_MERGE_IN_DECODE = 0, PA_MERGE_IN_REDUCE = 1 } pa_split_merge;
+
 /* Device-side input problems, OR-ed into the flags word. */
 enum {
   PA_FLAG_BAD_LENGTHS = 1,   /* q_lens[b] outside [0, max_q_len], context_lens[b] < q_lens[b],
@@ -99,8 +108,10 @@ typedef struct {
   int32_t kv_scale_mode;      /* pa_scale_mode; PA_SCALE_NONE unless kv_dtype is fp8 */
   int32_t causal;             /* 1: new token i sees keys up to its own position */
   float sm_scale;             /* logit scale, usually 1/sqrt(D) */
-  int32_t num_ctas;           /* persistent grid size; 0: SMs of the current device x grid_mult */
-  int32_t grid_mult;          /* CTAs per SM when num_ctas is 0; 0 means 1 */
+  int32_t num_ctas;           /* persistent grid size; 0: (SMs of the current device x grid_mult)
+                                 x the decode CTAs that fit on one SM */
+  int32_t grid_mult;          /* grid multiplier when num_ctas is 0; 0 means 1 */
+  int32_t split_merge;        /* pa_split_merge: where units cut into several pieces are merged */
 } pa_config;
 
 /* Bytes of workspace a pa_plan/pa_decode/pa_reduce sequence needs for cfg:
@@ -109,12 +120,12 @@ typedef struct {
  * May query the current device (num_ctas == 0).  Writes *bytes. */
 PA_API pa_status pa_workspace_size(const pa_config *cfg, size_t *bytes);
 
-/* Plan one decode step (device work, no host sync).  Reads context_lens[B],
- * q_lens[B] and block_tables[B][max_blocks_per_seq] (int32, row-major); checks
- * the lengths and every block id in use; writes the work list into ws.  Cuts the
+/* Plan one decode step (device work, no host sync).  Reads context_lens[B] and
+ * q_lens[B]; checks the lengths; writes the work list into ws.  Cuts the
  * concatenated token ranges of all (sequence, kv-head, row-block) units into C
  * contiguous tile-aligned pieces of equal size, one per CTA, so every CTA of the
- * persistent grid reads the same number of pages. */
+ * persistent grid reads the same number of pages.  block_tables is not read here
+ * (pa_decode checks every block id it uses) but must not be NULL. */
 PA_API pa_status pa_plan(const pa_config *cfg, const int32_t *block_tables, const int32_t *context_lens,
                   const int32_t *q_lens, void *ws, size_t ws_bytes, pa_stream stream);
 
@@ -131,8 +142,10 @@ PA_API pa_status pa_decode(const pa_config *cfg, const void *q, const void *k_ca
                     const int32_t *context_lens, const int32_t *q_lens, void *out, float *lse,
                     void *ws, size_t ws_bytes, pa_stream stream);
 
-/* Merge the split partials of every unit pa_decode left in ws into out (and lse),
- * and write the padding rows of units with no keys.  Completes the step. */
+/* Completes the step.  With PA_MERGE_IN_REDUCE: merges the split partials of every unit
+ * pa_decode left in ws into out (and lse) and writes the padding rows of units with no keys.
+ * With PA_MERGE_IN_DECODE pa_decode has already done both, and this call only validates its
+ * arguments and launches nothing. */
 PA_API pa_status pa_reduce(const pa_config *cfg, void *out, float *lse, void *ws, size_t ws_bytes,
                     pa_stream stream);
 

@@ -18,7 +18,8 @@ __all__ = ["PaConfig", "PaError", "load", "workspace_size", "plan", "decode", "r
            "decode_step_static", "STATIC_SCRATCH_BYTES",
            "read_flags", "status_string", "config_for", "paged_attention", "LIB_PATH",
            "BF16", "FP16", "FP8_E4M3", "SCALE_NONE", "SCALE_PER_TENSOR", "SCALE_PER_TOKEN",
-           "FLAG_BAD_LENGTHS", "FLAG_BAD_BLOCK_ID", "FLAG_WAIT_TIMEOUT", "EXPORTED_SYMBOLS"]
+           "FLAG_BAD_LENGTHS", "FLAG_BAD_BLOCK_ID", "FLAG_WAIT_TIMEOUT", "EXPORTED_SYMBOLS",
+           "MERGE_IN_DECODE", "MERGE_IN_REDUCE"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpa103.so")
@@ -29,6 +30,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = rang
 BF16, FP16, FP8_E4M3 = 0, 1, 2
 SCALE_NONE, SCALE_PER_TENSOR, SCALE_PER_TOKEN = 0, 1, 2
 FLAG_BAD_LENGTHS, FLAG_BAD_BLOCK_ID, FLAG_WAIT_TIMEOUT = 1, 2, 4
+MERGE_IN_DECODE, MERGE_IN_REDUCE = 0, 1
 
 EXPORTED_SYMBOLS = ("pa_workspace_size", "pa_plan", "pa_decode", "pa_reduce", "pa_read_flags",
                     "pa_status_string", "pa_decode_step_static")
@@ -42,7 +44,8 @@ class PaConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "max_q_len", "num_q_heads", "num_kv_heads", "head_dim", "block_size",
         "max_blocks_per_seq", "num_blocks", "q_dtype", "kv_dtype", "kv_scale_mode", "causal")] + [
-        ("sm_scale", ctypes.c_float), ("num_ctas", ctypes.c_int32), ("grid_mult", ctypes.c_int32)]
+        ("sm_scale", ctypes.c_float), ("num_ctas", ctypes.c_int32), ("grid_mult", ctypes.c_int32),
+        ("split_merge", ctypes.c_int32)]
 
 
 class PaError(RuntimeError):
@@ -156,7 +159,8 @@ _DT = {"bf16": BF16, "fp16": FP16, "fp8": FP8_E4M3}
 _SM = {"none": SCALE_NONE, "tensor": SCALE_PER_TENSOR, "token": SCALE_PER_TOKEN}
 
 
-def config_for(inp: dict, num_ctas: int = 0, grid_mult: int = 0) -> PaConfig:
+def config_for(inp: dict, num_ctas: int = 0, grid_mult: int = 0,
+               split_merge: int = MERGE_IN_DECODE) -> PaConfig:
     """pa_config of a problem laid out as workloads.make_inputs returns it."""
     w = inp["workload"]
     return PaConfig(batch=w.batch, max_q_len=w.max_q_len, num_q_heads=w.num_q_heads,
@@ -166,7 +170,7 @@ def config_for(inp: dict, num_ctas: int = 0, grid_mult: int = 0) -> PaConfig:
                     kv_dtype=_DT[w.kv_dtype],
                     kv_scale_mode=_SM[w.scale_mode] if w.kv_dtype == "fp8" else SCALE_NONE,
                     causal=int(w.causal), sm_scale=float(inp["sm_scale"]), num_ctas=num_ctas,
-                    grid_mult=grid_mult)
+                    grid_mult=grid_mult, split_merge=split_merge)
 
 
 def paged_attention(inp: dict, out=None, lse=None, ws=None, cfg: Optional[PaConfig] = None,

@@ -34,6 +34,8 @@ pa_status validate(const pa_config* c) {
   if (c->causal != 0 && c->causal != 1) return PA_ERR_INVALID_ARG;
   if (!std::isfinite(c->sm_scale)) return PA_ERR_INVALID_ARG;
   if (c->num_ctas < 0 || c->grid_mult < 0) return PA_ERR_INVALID_ARG;
+  if (c->split_merge != PA_MERGE_IN_DECODE && c->split_merge != PA_MERGE_IN_REDUCE)
+    return PA_ERR_INVALID_ARG;
   if (c->num_q_heads % c->num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return PA_ERR_UNSUPPORTED;
   if (!is_pow2(c->block_size) || c->block_size < 16 || c->block_size > 1024)
@@ -46,7 +48,9 @@ pa_status validate(const pa_config* c) {
   return PA_OK;
 }
 
-pa_status resolve_ctas(const pa_config& c, int* ctas) {
+// Persistent grid: num_ctas if given, else (SMs x grid_mult) x the decode CTAs that fit
+// on one SM, so the whole grid is resident at once.
+pa_status resolve_ctas(const pa_config& c, const Variant& v, int* ctas) {
   if (c.num_ctas > 0) {
     *ctas = c.num_ctas > 65535 ? 65535 : c.num_ctas;
     return PA_OK;
@@ -56,7 +60,7 @@ pa_status resolve_ctas(const pa_config& c, int* ctas) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PA_ERR_CUDA;
   const int mult = c.grid_mult > 0 ? c.grid_mult : 1;
-  long long n = (long long)sms * mult;
+  long long n = (long long)sms * mult * v.ctas_per_sm;
   *ctas = (int)(n > 65535 ? 65535 : n);
   return PA_OK;
 }
@@ -64,10 +68,9 @@ pa_status resolve_ctas(const pa_config& c, int* ctas) {
 pa_status prepare(const pa_config* cfg, Variant* v, WsLayout* L) {
   pa_status st = validate(cfg);
   if (st != PA_OK) return st;
-  int ctas = 0;
-  st = resolve_ctas(*cfg, &ctas);
+  *v = make_variant(*cfg);
+  st = resolve_ctas(*cfg, *v, &v->ctas);
   if (st != PA_OK) return st;
-  *v = make_variant(*cfg, ctas);
   // The planner's concatenated token space is indexed with int32.
   const long long per_unit = (long long)round_up(cfg->max_blocks_per_seq, 1) * cfg->block_size + v->tt;
   if ((long long)v->units * per_unit >= (1ll << 30)) return PA_ERR_UNSUPPORTED;
@@ -208,6 +211,7 @@ pa_status pa_decode(const pa_config* cfg, const void* q, const void* k_cache, co
   a.v = v;
   a.q_kind = cfg->q_dtype == PA_FP16 ? Q_FP16 : Q_BF16;
   a.kv_kind = cfg->kv_dtype == PA_FP8_E4M3 ? KV_FP8 : cfg->kv_dtype == PA_FP16 ? KV_FP16 : KV_BF16;
+  a.merge_in_decode = cfg->split_merge == PA_MERGE_IN_DECODE;
   cudaError_t e = launch_decode_simt(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -222,6 +226,7 @@ pa_status pa_reduce(const pa_config* cfg, void* out, float* lse, void* ws, size_
   if (!out || !aligned(out, 16)) return PA_ERR_INVALID_ARG;
   if (lse && !aligned(lse, 4)) return PA_ERR_INVALID_ARG;
   if ((st = check_ws(ws, ws_bytes, L)) != PA_OK) return st;
+  if (cfg->split_merge == PA_MERGE_IN_DECODE) return PA_OK;  // pa_decode finished the step
   DecodeArgs a{};
   a.p = problem_args(*cfg, nullptr, nullptr, nullptr);
   a.out = out;

@@ -1,26 +1,28 @@
 // Persistent split-KV paged decode on CUDA cores, for query tiles of at most 8 rows.
 //
-// Page gather.  One producer warp streams the KV pages of its CTA's work items into a
-// 4-stage shared-memory ring: for every tile of TT tokens it looks up the physical block of
-// each page through the block table and issues one 4-D TMA box (D x 1 head x rows x 1
-// block) per page for K and one for V, completing on the stage's mbarrier.  While the
-// consumers work on stage s, the next three stages are in flight.  This is the GB300 form
-// of the K/V ping-pong of "HSTU Paged Attention" (RecSDK issue 1281, optimisation plan:
-// split the buffer into K/V tensors and two ping-pong stages, overlap the next chunk's load
-// with the current chunk's use, chunk capacity derived from the buffer budget and D); here
-// the buffer is shared memory, the copy engine is TMA, and the stage count is four.
+// Page gather.  Warp 0 streams the KV pages of its CTA's work items into a 3-stage
+// shared-memory ring while it also computes: for every tile of TT tokens it looks up the
+// physical block of each page through the block table and issues one 4-D TMA box
+// (D x 1 head x rows x 1 block) per page for K and one for V, completing on the stage's
+// mbarrier; the next tile's block ids are fetched while the current tile is in flight.
+// While the CTA works on stage s the next two stages are loading, and two CTAs share each
+// SM, so four tiles per SM are always in flight.  This is the GB300 form of the K/V
+// ping-pong of "HSTU Paged Attention" (RecSDK issue 1281, optimisation plan: K/V buffers in
+// two ping-pong stages, the next chunk's load overlapping the current chunk's use, the chunk
+// capacity derived from the buffer budget and D): the buffer is shared memory, the copy
+// engine is TMA and the ring is deeper.
 //
-// Math.  Eight consumer warps split each tile's tokens between token groups of LPT lanes;
-// each lane owns DPL = D / LPT dimensions of every query row.  Per token a group forms the
-// MP partial dot products, reduce-scatters them across its lanes with warp shuffles (each
-// lane ends with one row's logit), updates that row's running max and sum, and broadcasts
-// the MP softmax weights back for the P.V accumulation.  Each group keeps its own online
-// softmax state, so groups never wait on one another inside an item; the states are merged
-// with the log-sum-exp rule when the item ends (first across the groups of a warp with
-// shuffles, then across warps through shared memory).  The running max is only moved when a
-// logit exceeds it by more than 2^8 (logits are kept in log2 units), which keeps the
-// rescale of the accumulators off the common path; the final normalisation uses the same
-// reference max, so the result is exact up to rounding.
+// Math.  The CTA's four warps split each tile's tokens between token groups of LPT lanes;
+// a lane owns DPL = D / LPT dimensions of every query row.  A group takes two tokens per
+// step: the 2 * MP partial dot products (packed fp32x2 FMA) are reduce-scattered across
+// the group's lanes with warp shuffles so that each lane ends with one (token, row) logit;
+// the two lanes of a row agree on its running max, each exponentiates its own logit, and
+// the 2 * MP weights are broadcast back for the P.V accumulation (packed FMA again).  Each
+// group keeps its own online-softmax state, merged with the log-sum-exp rule when an item
+// ends (across the groups of a warp with shuffles, then across warps through shared
+// memory).  Logits are in log2 units and the running max is only moved when a logit beats
+// it by more than 2^8, which keeps the accumulator rescale off the common path; the final
+// normalisation uses the same reference max, so the result is exact up to rounding.
 //
 // fp8 caches are dequantised in registers (E4M3 pairs to half2 to float); a per-tensor K
 // scale is folded into the query, a per-tensor V scale into the final normalisation, and
@@ -49,105 +51,117 @@ struct SimtParams {
   float* o_part;
   float* lse_part;
   int32_t* flags;
+  const int2* unit_info;
+  int32_t* unit_cnt;
+  int units;
+  int merge_in_decode;
   int scale_mode;
   int Sq, Hq, Hkv, G, M, RB, bs, maxb, nblocks, causal;
+  int bs_shift;  // log2(bs): pages are a power of two
   float qk_scale;
 };
+
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 template <int D, int MP, int KVK, bool TOKS>
 struct SimtTraits {
   static constexpr int BPE = KVK == KV_FP8 ? 1 : 2;
-  static constexpr int DPL = MP <= 4 ? 16 : 8;  // dims per lane
-  static constexpr int LPT = D / DPL;            // lanes per token group
-  static constexpr int GPW = 32 / LPT;           // token groups per warp
-  static constexpr int NCW = 8;                  // consumer warps
-  static constexpr int NG = NCW * GPW;           // token groups per CTA
-  static constexpr int NTHREADS = (NCW + 1) * 32;
+  static constexpr int LPT0 = cmax(D / 16, 2 * MP);
+  static constexpr int LPT = (MP * (D / LPT0) > 64) ? 2 * LPT0 : LPT0;  // lanes per token group
+  static constexpr int DPL = D / LPT;                                    // dims per lane
+  static constexpr int GPW = 32 / LPT;                                   // groups per warp
+  static constexpr int NW = 4;                                           // warps per CTA
+  static constexpr int NG = NW * GPW;                                    // groups per CTA
+  static constexpr int NTHREADS = NW * 32;
+  static constexpr int NV = 2 * MP;           // values per group step: 2 tokens x MP rows
+  static constexpr int RSTRIDE = LPT / NV;    // lanes holding one value after the scatter
   static constexpr int TT = kTileBytes / (D * BPE);  // tokens per stage
-  static constexpr int NSTAGE = 4;
-  static constexpr int CB = DPL * BPE < 16 ? DPL * BPE : 16;  // bytes per chunk
-  static constexpr int EPC = CB / BPE;                         // elements per chunk
-  static constexpr int CH = DPL / EPC;                         // chunks per lane
-  static constexpr int RSTRIDE = LPT / MP;  // lanes holding one row after the reduce-scatter
+  static constexpr int NSTAGE = 3;
+  static constexpr int NQ = NSTAGE;           // query slots (one per item a stage can start)
+  static constexpr int CB = cmin(16, DPL * BPE);  // bytes per chunk
+  static constexpr int EPC = CB / BPE;            // elements per chunk
+  static constexpr int CH = DPL / EPC;            // chunks per lane
   static constexpr int KTILE = TT * D * BPE;
   static constexpr int STAGE = round_up(2 * KTILE + (TOKS ? 2 * TT * 4 : 0), 1024);
-  static constexpr int QHDR = 128;
-  static constexpr int QSLOT = round_up(QHDR + MP * D * 2, 128);
-  static constexpr int MERGE = NCW * MP * D * 4 + 2 * NCW * MP * 4;
+  static constexpr int QSLOT = round_up(MP * D * 2, 128);
+  // The item-end merge needs the warps' accumulators (MERGE_O) and running max and sum
+  // (MERGE_ML).  The accumulators get their own buffer when two CTAs still fit on an SM;
+  // otherwise they borrow the stage of the item's last tile, released after the merge.
+  static constexpr int MERGE_O = NW * MP * D * 4;
+  static constexpr int MERGE_ML = 2 * NW * MP * 4;
   static constexpr int OFF_Q = NSTAGE * STAGE;
-  static constexpr int OFF_MERGE = OFF_Q + 2 * QSLOT;
-  static constexpr int OFF_BAR = round_up(OFF_MERGE + MERGE, 64);
-  static constexpr int NBAR = 2 * NSTAGE + 4;
+  static constexpr int BASE_BYTES = OFF_Q + NQ * QSLOT + MERGE_ML + 64 + (2 * NSTAGE + NQ) * 8 + 16 + 1024;
+  static constexpr bool OWN_MERGE = 2 * (BASE_BYTES + MERGE_O + 1024) <= 228 * 1024;
+  static constexpr int OFF_MERGE = OFF_Q + NQ * QSLOT;
+  static constexpr int OFF_MERGE_O = OFF_MERGE + MERGE_ML;
+  static constexpr int OFF_BAR = round_up(OFF_MERGE_O + (OWN_MERGE ? MERGE_O : 0), 64);
+  static constexpr int NBAR = 2 * NSTAGE + NQ;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
-  static_assert(MP <= LPT && LPT <= 32 && 32 % LPT == 0, "row tile vs lanes");
-  static_assert(DPL % EPC == 0 && TT % 32 == 0 && TT <= 256, "tile shape");
+  static constexpr int CTAS_PER_SM = 2 * (SMEM + 1024) <= 228 * 1024 ? 2 : 1;
+  static_assert(NV <= LPT && LPT <= 32 && 32 % LPT == 0, "row tile vs lanes");
+  static_assert(DPL % EPC == 0 && EPC % 2 == 0, "chunking");
+  static_assert(MERGE_O <= STAGE, "merge buffer must fit in one stage");
+  static_assert(TT % 32 == 0 && TT <= 256, "tile shape");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // ---- element conversion -----------------------------------------------------------
-__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float* f) {
-  f[0] = __uint_as_float(w << 16);
-  f[1] = __uint_as_float(w & 0xffff0000u);
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
-__device__ __forceinline__ void f16x2_to_f32(uint32_t w, float* f) {
-  __half2 h = *reinterpret_cast<__half2*>(&w);
-  float2 r = __half22float2(h);
-  f[0] = r.x;
-  f[1] = r.y;
+__device__ __forceinline__ float2 f16x2_to_f2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<__half2*>(&w));
 }
-__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float* f) {
+__device__ __forceinline__ void e4m3x4_to_f2(uint32_t w, float2* f) {
   __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
   __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
-  float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
-  float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
-  f[0] = a.x;
-  f[1] = a.y;
-  f[2] = b.x;
-  f[3] = b.y;
+  f[0] = __half22float2(*reinterpret_cast<__half2*>(&lo));
+  f[1] = __half22float2(*reinterpret_cast<__half2*>(&hi));
 }
 
-// Load one chunk of EPC cache elements from shared memory as floats.
-template <int KVK, int EPC>
-__device__ __forceinline__ void load_kv_chunk(const char* src, float* f) {
-  if constexpr (KVK == KV_FP8) {
-    if constexpr (EPC == 16) {
-      const uint4 w = *reinterpret_cast<const uint4*>(src);
-      e4m3x4_to_f32(w.x, f);
-      e4m3x4_to_f32(w.y, f + 4);
-      e4m3x4_to_f32(w.z, f + 8);
-      e4m3x4_to_f32(w.w, f + 12);
-    } else {
-      const uint2 w = *reinterpret_cast<const uint2*>(src);
-      e4m3x4_to_f32(w.x, f);
-      e4m3x4_to_f32(w.y, f + 4);
-    }
+// Raw chunk of cache elements in registers: CB bytes = CB / 4 words.
+template <int CB>
+struct RawChunk {
+  uint32_t w[CB / 4];
+};
+
+template <int CB>
+__device__ __forceinline__ RawChunk<CB> lds_chunk(const char* src) {
+  RawChunk<CB> r;
+  if constexpr (CB == 16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+  } else if constexpr (CB == 8) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    r.w[0] = v.x; r.w[1] = v.y;
   } else {
-    const uint4 w = *reinterpret_cast<const uint4*>(src);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    r.w[0] = *reinterpret_cast<const uint32_t*>(src);
+  }
+  return r;
+}
+
+// Convert a raw chunk of EPC elements to EPC / 2 float2 pairs (element order kept).
+template <int KVK, int CB>
+__device__ __forceinline__ void chunk_to_f2(const RawChunk<CB>& r, float2* f) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if constexpr (KVK == KV_BF16)
-        bf16x2_to_f32(ws[j], f + 2 * j);
-      else
-        f16x2_to_f32(ws[j], f + 2 * j);
+  for (int j = 0; j < CB / 4; ++j) {
+    if constexpr (KVK == KV_FP8) {
+      e4m3x4_to_f2(r.w[j], f + 2 * j);
+    } else if constexpr (KVK == KV_BF16) {
+      f[j] = bf16x2_to_f2(r.w[j]);
+    } else {
+      f[j] = f16x2_to_f2(r.w[j]);
     }
   }
 }
 
-// Load n 16-bit query elements (n a multiple of 8) from shared memory as floats.
 template <int QK>
-__device__ __forceinline__ void load_q_elems(const char* src, int n, float* f) {
-  for (int c = 0; c < n / 8; ++c) {
-    const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * c);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if constexpr (QK == Q_BF16)
-        bf16x2_to_f32(ws[j], f + 8 * c + 2 * j);
-      else
-        f16x2_to_f32(ws[j], f + 8 * c + 2 * j);
-    }
-  }
+__device__ __forceinline__ float2 q_pair(uint32_t w) {
+  if constexpr (QK == Q_BF16)
+    return bf16x2_to_f2(w);
+  else
+    return f16x2_to_f2(w);
 }
 
 template <int QK>
@@ -159,31 +173,370 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
 }
 
 // Reduce-scatter of N values over the lanes of a token group, starting at lane offset OFF
-// (= LPT / 2): after it, lane l of the group holds in v[0] the group sum of value
-// number l / (LPT / N).
+// (= LPT / 2).  Each lane keeps its values in a lane-specific order: position p holds value
+// p XOR v_own, where v_own = (lane within the group) / (LPT / N).  With that order every lane
+// keeps the lower half and sends the upper half at each halving step, and the partner's
+// upper-half entry is the same value, so a step is N / 2 shuffles and adds with no selects.
+// Afterwards v[0] holds the group sum of value v_own.
 template <int N, int OFF>
-__device__ __forceinline__ void reduce_scatter(float* v, int lane) {
+__device__ __forceinline__ void reduce_scatter(float* v) {
   if constexpr (OFF > 0) {
     if constexpr (N > 1) {
-      const bool upper = (lane & OFF) != 0;
 #pragma unroll
-      for (int j = 0; j < N / 2; ++j) {
-        const float send = upper ? v[j] : v[j + N / 2];
-        const float keep = upper ? v[j + N / 2] : v[j];
-        v[j] = keep + __shfl_xor_sync(kFull, send, OFF);
-      }
-      reduce_scatter<N / 2, OFF / 2>(v, lane);
+      for (int j = 0; j < N / 2; ++j) v[j] += __shfl_xor_sync(kFull, v[j + N / 2], OFF);
+      reduce_scatter<N / 2, OFF / 2>(v);
     } else {
       v[0] += __shfl_xor_sync(kFull, v[0], OFF);
-      reduce_scatter<1, OFF / 2>(v, lane);
+      reduce_scatter<1, OFF / 2>(v);
     }
   }
 }
 
 constexpr float kRescaleSlack = 8.0f;  // log2 units: weights stay <= 2^8 between rescales
 
+// The TMA side of the ring, run by warp 0 (all lanes, same state) between its own tiles.
+template <int D, int MP, int KVK, bool TOKS>
+struct TileProducer {
+  using T = SimtTraits<D, MP, KVK, TOKS>;
+  const SimtParams* p;
+  const CUtensorMap* kmap;
+  const CUtensorMap* vmap;
+  char* smem;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* qfull;
+  volatile int* abort_flag;
+  int lane, it, it_end;
+  int k, ntiles, t0, t1, b, g, rb;
+  uint32_t issued, items_started;
+  int box_rows, nbox;
+  uint32_t box_bytes;
+  int blk_next;
+  bool have;        // current item has tiles left
+  bool next_ready;  // blk_next already holds the next item's first-tile block ids
+  int4 item_next;
+
+  __device__ __forceinline__ int box_block_of(int bb, int tt0, int tt1, int kk) const {
+    const int tokb = tt0 + kk * T::TT + lane * box_rows;
+    return (lane < nbox && tokb < tt1) ? __ldg(p->bt + (size_t)bb * p->maxb + (tokb >> p->bs_shift)) : -1;
+  }
+  __device__ __forceinline__ int box_block(int kk) const { return box_block_of(b, t0, t1, kk); }
+
+  __device__ __forceinline__ void init(const SimtParams* prm, const CUtensorMap* km,
+                                       const CUtensorMap* vm, char* sm, uint64_t* f,
+                                       uint64_t* e, uint64_t* qf, volatile int* ab, int ln,
+                                       int ib, int ie) {
+    p = prm; kmap = km; vmap = vm; smem = sm; full = f; empty = e; qfull = qf; abort_flag = ab;
+    lane = ln; it = ib - 1; it_end = ie; k = 0; ntiles = 0; issued = 0; items_started = 0;
+    box_rows = min(p->bs, T::TT);
+    nbox = T::TT / box_rows;
+    box_bytes = (uint32_t)box_rows * D * T::BPE;
+    have = false;
+    next_ready = false;
+    item_next = ib < ie ? p->items[ib] : make_int4(0, 0, 0, -1);
+  }
+
+  // Move to the next item with tokens; false when the CTA's list is exhausted.
+  __device__ __forceinline__ bool advance() {
+    while (!have) {
+      if (++it >= it_end) return false;
+      const int4 item = item_next;
+      if (it + 1 < it_end) item_next = p->items[it + 1];
+      t0 = item.y;
+      t1 = item.z;
+      if (t1 <= t0) continue;
+      const int u = item.x;
+      b = u / (p->Hkv * p->RB);
+      g = (u / p->RB) % p->Hkv;
+      rb = u % p->RB;
+      k = 0;
+      ntiles = ceil_div(t1 - t0, T::TT);
+      if (!next_ready) blk_next = box_block(0);
+      next_ready = false;
+      have = true;
+    }
+    return true;
+  }
+
+  // Issue the next tile of the CTA's sequence into its stage (waiting for the stage to be
+  // released by every warp); the query rows of an item go out with its first tile.
+  __device__ __forceinline__ bool issue_one() {
+    if (!advance()) return false;
+    const int s = issued % T::NSTAGE;
+    const uint32_t ph = (issued / T::NSTAGE) & 1;
+    const int tok0 = t0 + k * T::TT;
+    const int tokb = tok0 + lane * box_rows;
+    const int blk = blk_next;
+    const bool want = lane < nbox && tokb < t1;
+    const bool ok = want && blk >= 0 && blk < p->nblocks;
+    if (want && !ok) atomicOr(p->flags, PA_FLAG_BAD_BLOCK_ID);
+    const uint32_t nvalid = __popc(__ballot_sync(kFull, ok));
+    // overlap the next lookup: the next tile of this item, or the first of the next item
+    if (k + 1 < ntiles) {
+      blk_next = box_block(k + 1);
+    } else if (it + 1 < it_end && item_next.z > item_next.y) {
+      blk_next = box_block_of(item_next.x / (p->Hkv * p->RB), item_next.y, item_next.z, 0);
+      next_ready = true;
+    }
+    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+      atomicOr(p->flags, PA_FLAG_WAIT_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+    if (k == 0) {
+      // query rows of this item: MP rows x D, 16-byte cp.async, completing on qfull
+      const int qs = items_started % T::NQ;
+      ++items_started;
+      char* qslot = smem + T::OFF_Q + qs * T::QSLOT;
+      constexpr int QCH = D * 2 / 16;
+      for (int c = lane; c < MP * QCH; c += 32) {
+        const int r = c / QCH, cc = c % QCH, rg = rb * MP + r;
+        if (rg < p->M) {
+          const int i = rg / p->G, gq = rg % p->G;
+          const char* src = reinterpret_cast<const char*>(p->q) +
+                            ((((size_t)b * p->Sq + i) * p->Hq + (size_t)g * p->G + gq) * D) * 2 +
+                            cc * 16;
+          cp_async_16(qslot + r * D * 2 + cc * 16, src);
+        }
+      }
+      cp_async_arrive_noinc(&qfull[qs]);
+    }
+    char* st = smem + s * T::STAGE;
+    if (lane == 0) mbar_arrive_expect_tx(&full[s], nvalid * 2u * box_bytes);
+    __syncwarp();
+    if (ok) {
+      const int row = tokb & (p->bs - 1);
+      tma_load_4d(st + lane * box_bytes, kmap, &full[s], 0, g, row, blk);
+      tma_load_4d(st + T::KTILE + lane * box_bytes, vmap, &full[s], 0, g, row, blk);
+    }
+    if constexpr (TOKS) {
+      float* sks = reinterpret_cast<float*>(st + 2 * T::KTILE);
+      float* svs = sks + T::TT;
+      for (int t = lane; t < T::TT; t += 32) {
+        const int bb = __shfl_sync(kFull, blk, t / box_rows);
+        const int tok = tok0 + t;
+        if (tok < t1 && bb >= 0 && bb < p->nblocks) {
+          const size_t idx = ((size_t)bb * p->bs + (tok & (p->bs - 1))) * p->Hkv + g;
+          cp_async_4(sks + t, p->k_scale + idx);
+          cp_async_4(svs + t, p->v_scale + idx);
+        }
+      }
+      cp_async_arrive_noinc(&full[s]);
+    }
+    ++issued;
+    if (++k >= ntiles) have = false;
+    return true;
+  }
+
+  // Keep the ring filled up to tile `upto` (global tile index of this CTA).
+  __device__ __forceinline__ void fill(uint32_t upto) {
+    while (issued <= upto && !*abort_flag) {
+      if (!issue_one()) break;
+    }
+  }
+
+  // Let every copy this warp started land before the CTA may exit.
+  __device__ __forceinline__ void drain() {
+    cp_async_wait_all();
+    const uint32_t first = issued > (uint32_t)T::NSTAGE ? issued - T::NSTAGE : 0;
+    for (uint32_t j = first; j < issued; ++j)
+      mbar_wait_drain(&full[j % T::NSTAGE], (j / T::NSTAGE) & 1);
+  }
+};
+
+// Per-tile context of a consumer lane.
+template <int D, int MP, int KVK, bool TOKS>
+struct StepCtx {
+  const char* ks;     // K tile [TT][D]
+  const char* vs;     // V tile [TT][D]
+  const float* sks;   // per-token K scales [TT] (per-token mode)
+  const float* svs;   // per-token V scales [TT]
+  int tok0;           // first token of the tile
+  int n_in;           // valid tokens in the tile
+  int limit_own;      // keys visible to this lane's row
+  int lg, gbase, tk_own;
+};
+
+// One step of a token group: tokens ta and ta + 1 of the tile.  The lane accumulates the
+// token it owns after the reduce-scatter first (tk_own), so its partials are already in the
+// scatter order: position tk * MP + r holds token (tk ^ tk_own), row (r ^ r_own).
+template <bool CHECK, int D, int MP, int KVK, bool TOKS>
+__device__ __forceinline__ void token_step(const StepCtx<D, MP, KVK, TOKS>& cx, int ta,
+                                           const float2 (&q)[MP][SimtTraits<D, MP, KVK, TOKS>::DPL / 2],
+                                           float2 (&o)[MP][SimtTraits<D, MP, KVK, TOKS>::DPL / 2],
+                                           float& m_run, float& l_own) {
+  using T = SimtTraits<D, MP, KVK, TOKS>;
+  constexpr int PAIR = MP * T::RSTRIDE;  // lane distance to the same row's other token
+  const int tb = ta + 1;
+  const bool va = !CHECK || ta < cx.n_in, vb = !CHECK || tb < cx.n_in;
+  // this lane's own token first
+  const int t_first = cx.tk_own ? tb : ta, t_second = cx.tk_own ? ta : tb;
+  const bool v_first = cx.tk_own ? vb : va, v_second = cx.tk_own ? va : vb;
+  const int tl_first = (!CHECK || v_first) ? t_first : 0;
+  const int tl_second = (!CHECK || v_second) ? t_second : 0;
+  float acc[T::NV];
+  {
+    float2 s1[MP], s2[MP];
+#pragma unroll
+    for (int r = 0; r < MP; ++r) s1[r] = s2[r] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < T::CH; ++c) {
+      const int off = (cx.lg + c * T::LPT) * T::CB;
+      const RawChunk<T::CB> r1 = lds_chunk<T::CB>(cx.ks + (size_t)tl_first * D * T::BPE + off);
+      const RawChunk<T::CB> r2 = lds_chunk<T::CB>(cx.ks + (size_t)tl_second * D * T::BPE + off);
+      float2 f1[T::EPC / 2], f2[T::EPC / 2];
+      chunk_to_f2<KVK, T::CB>(r1, f1);
+      chunk_to_f2<KVK, T::CB>(r2, f2);
+#pragma unroll
+      for (int e = 0; e < T::EPC / 2; ++e) {
+#pragma unroll
+        for (int r = 0; r < MP; ++r) {
+          s1[r] = ffma2(q[r][c * T::EPC / 2 + e], f1[e], s1[r]);
+          s2[r] = ffma2(q[r][c * T::EPC / 2 + e], f2[e], s2[r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < MP; ++r) {
+      acc[r] = s1[r].x + s1[r].y;
+      acc[MP + r] = s2[r].x + s2[r].y;
+    }
+  }
+  reduce_scatter<T::NV, T::LPT / 2>(acc);
+  // this lane's (token, row) logit, masked
+  float sc = acc[0];
+  if constexpr (TOKS) sc *= cx.sks[tl_first];
+  sc = ((!CHECK || v_first) && cx.tok0 + t_first < cx.limit_own) ? sc : -INFINITY;
+  // the two lanes of a row agree on its running max
+  const float s_pair = fmaxf(sc, __shfl_xor_sync(kFull, sc, PAIR));
+  const bool need = s_pair > m_run + kRescaleSlack;
+  if (__any_sync(kFull, need)) {
+    const float mn = need ? s_pair : m_run;
+    const float alpha = (mn == m_run) ? 1.f : fast_exp2(m_run - mn);
+    l_own *= alpha;
+    m_run = mn;
+#pragma unroll
+    for (int r = 0; r < MP; ++r) {
+      const float a = __shfl_sync(kFull, alpha, cx.gbase + r * T::RSTRIDE);
+#pragma unroll
+      for (int d = 0; d < T::DPL / 2; ++d) {
+        o[r][d].x *= a;
+        o[r][d].y *= a;
+      }
+    }
+  }
+  const float pr = (sc == -INFINITY) ? 0.f : fast_exp2(sc - m_run);
+  l_own += pr;
+  float pv = pr;
+  if constexpr (TOKS) pv *= cx.svs[tl_first];
+  float pw[T::NV];  // weights by value: token a rows, then token b rows
+#pragma unroll
+  for (int v = 0; v < T::NV; ++v) pw[v] = __shfl_sync(kFull, pv, cx.gbase + v * T::RSTRIDE);
+  // P.V for both tokens (an invalid token has weight 0 and is skipped)
+#pragma unroll
+  for (int c = 0; c < T::CH; ++c) {
+    const int off = (cx.lg + c * T::LPT) * T::CB;
+    float2 fa[T::EPC / 2], fb[T::EPC / 2];
+    if (!CHECK || va) {
+      const RawChunk<T::CB> ra = lds_chunk<T::CB>(cx.vs + (size_t)ta * D * T::BPE + off);
+      chunk_to_f2<KVK, T::CB>(ra, fa);
+    } else {
+#pragma unroll
+      for (int e = 0; e < T::EPC / 2; ++e) fa[e] = make_float2(0.f, 0.f);
+    }
+    if (!CHECK || vb) {
+      const RawChunk<T::CB> rb2 = lds_chunk<T::CB>(cx.vs + (size_t)tb * D * T::BPE + off);
+      chunk_to_f2<KVK, T::CB>(rb2, fb);
+    } else {
+#pragma unroll
+      for (int e = 0; e < T::EPC / 2; ++e) fb[e] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < MP; ++r) {
+      const float2 wa = make_float2(pw[r], pw[r]);
+      const float2 wb = make_float2(pw[MP + r], pw[MP + r]);
+#pragma unroll
+      for (int e = 0; e < T::EPC / 2; ++e) {
+        o[r][c * T::EPC / 2 + e] = ffma2(wa, fa[e], o[r][c * T::EPC / 2 + e]);
+        o[r][c * T::EPC / 2 + e] = ffma2(wb, fb[e], o[r][c * T::EPC / 2 + e]);
+      }
+    }
+  }
+}
+
+// The split merge inside the decode kernel: after a CTA has written its partial of unit u,
+// it counts itself in; the CTA that brings the count to the number of pieces merges every
+// piece of the unit (its own last) with the log-sum-exp rule and writes the output.  No CTA
+// waits for another: the ones that are not last simply move on.  The fences order each
+// CTA's partial writes before its arrival and the merging CTA's reads after it; partials are
+// read through L2 (ld.global.cg), where other SMs' writes are visible.
+template <int D, int MP, int QK, int NW>
+__device__ __forceinline__ void merge_if_last(const SimtParams& p, int u, int b, int g, int rb,
+                                              float* wtab, int wcap, float* stat,
+                                              volatile int* last_flag) {
+  constexpr int NT = NW * 32;
+  const int2 info = __ldg(&p.unit_info[u]);
+  const int first = info.x, ns = info.y;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int before = atomicAdd(&p.unit_cnt[u], 1);
+    *last_flag = before == ns - 1;
+  }
+  named_barrier_sync(1, NT);
+  if (!*last_flag) return;
+  __threadfence();
+  const bool tab = MP * ns <= wcap;  // weights fit in shared memory
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // per row: max and weight sum over the pieces (lanes over pieces)
+  for (int r = warp; r < MP; r += NW) {
+    float m = -INFINITY;
+    for (int s = lane; s < ns; s += 32)
+      m = fmaxf(m, __ldcg(p.lse_part + (size_t)piece_slot(first, s) * MP + r));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    float W = 0.f;
+    for (int s = lane; s < ns; s += 32) {
+      const float ls = __ldcg(p.lse_part + (size_t)piece_slot(first, s) * MP + r);
+      const float w = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+      if (tab) wtab[r * ns + s] = w;
+      W += w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
+    if (lane == 0) {
+      stat[2 * r] = m;
+      stat[2 * r + 1] = W;
+    }
+  }
+  named_barrier_sync(1, NT);
+  for (int e = threadIdx.x; e < MP * D; e += NT) {
+    const int r = e / D, d = e % D, rg = rb * MP + r;
+    if (rg >= p.M) continue;
+    const float m = stat[2 * r], W = stat[2 * r + 1];
+    float O = 0.f;
+    if (W > 0.f) {
+#pragma unroll 4
+      for (int s = 0; s < ns; ++s) {
+        const size_t part = (size_t)piece_slot(first, s) * MP + r;
+        float w;
+        if (tab) {
+          w = wtab[r * ns + s];
+        } else {
+          const float ls = __ldcg(p.lse_part + part);
+          w = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+        }
+        O += w * __ldcg(p.o_part + part * D + d);
+      }
+    }
+    const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
+    store_out<QK>(p.out, row * D + d, W > 0.f ? O / W : 0.f);
+    if (d == 0 && p.lse) p.lse[row] = W > 0.f ? (m + fast_log2(W)) * kLn2 : -INFINITY;
+  }
+  named_barrier_sync(1, NT);  // the shared buffers are reused by the next item
+}
+
 template <int D, int MP, int KVK, int QK, bool TOKS>
-__global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 1)
+__global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
     decode_simt_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const SimtParams p) {
   using T = SimtTraits<D, MP, KVK, TOKS>;
@@ -192,186 +545,111 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   uint64_t* empty = full + T::NSTAGE;
   uint64_t* qfull = empty + T::NSTAGE;
-  uint64_t* qempty = qfull + 2;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(qempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(qfull + T::NQ);
+  volatile int* last_flag = abort_flag + 1;  // this CTA finished the last piece of a unit
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < T::NSTAGE; ++s) {
       mbar_init(&full[s], TOKS ? 33 : 1);
-      mbar_init(&empty[s], T::NCW);
+      mbar_init(&empty[s], T::NW);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&qfull[s], 32);
-      mbar_init(&qempty[s], T::NCW);
-    }
+    for (int s = 0; s < T::NQ; ++s) mbar_init(&qfull[s], 32);
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
   __syncthreads();
+  grid_dependency_wait();  // the work list comes from the planner launched just before
 
   const int it_begin = p.item_off[blockIdx.x], it_end = p.item_off[blockIdx.x + 1];
-
-  if (warp == T::NCW) {
-    // ------------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-    }
-    const int box_rows = min(p.bs, T::TT);
-    const int nbox = T::TT / box_rows;
-    const uint32_t box_bytes = (uint32_t)box_rows * D * T::BPE;
-    uint32_t tile_ctr = 0, item_ctr = 0;
-    bool running = true;
-    for (int it = it_begin; it < it_end && running; ++it) {
-      const int4 item = p.items[it];
-      const int u = item.x, t0 = item.y, t1 = item.z;
-      const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
-      const int qs = item_ctr & 1;
-      const uint32_t qph = (item_ctr >> 1) & 1;
-      ++item_ctr;
-      if (!mbar_wait(&qempty[qs], qph ^ 1, abort_flag)) {
-        atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
-        *abort_flag = 1;
-        break;
-      }
-      char* qslot = smem + T::OFF_Q + qs * T::QSLOT;
-      if (t1 > t0) {
-        if (lane == 0) cp_async_4(qslot + 16, p.ctx + b);
-        if (lane == 1) cp_async_4(qslot + 20, p.qlens + b);
-        constexpr int QCH = D * 2 / 16;  // 16-byte chunks per query row
-        for (int c = lane; c < MP * QCH; c += 32) {
-          const int r = c / QCH, cc = c % QCH, rg = rb * MP + r;
-          if (rg < p.M) {
-            const int i = rg / p.G, gq = rg % p.G;
-            const char* src = reinterpret_cast<const char*>(p.q) +
-                              ((((size_t)b * p.Sq + i) * p.Hq + (size_t)g * p.G + gq) * D) * 2 +
-                              cc * 16;
-            cp_async_16(qslot + T::QHDR + r * D * 2 + cc * 16, src);
-          }
-        }
-      }
-      cp_async_arrive_noinc(&qfull[qs]);
-      if (t1 <= t0) continue;
-
-      const int ntiles = ceil_div(t1 - t0, T::TT);
-      const int32_t* btrow = p.bt + (size_t)b * p.maxb;
-      auto box_block = [&](int k) {
-        const int tokb = t0 + k * T::TT + lane * box_rows;
-        return (lane < nbox && tokb < t1) ? __ldg(btrow + tokb / p.bs) : -1;
-      };
-      int blk_next = box_block(0);
-      for (int k = 0; k < ntiles; ++k) {
-        const int s = tile_ctr % T::NSTAGE;
-        const uint32_t ph = (tile_ctr / T::NSTAGE) & 1;
-        const int tok0 = t0 + k * T::TT;
-        const int tokb = tok0 + lane * box_rows;
-        const int blk = blk_next;
-        const bool want = lane < nbox && tokb < t1;
-        const bool ok = want && blk >= 0 && blk < p.nblocks;
-        if (want && !ok) atomicOr(p.flags, PA_FLAG_BAD_BLOCK_ID);
-        const uint32_t nvalid = __popc(__ballot_sync(kFull, ok));
-        if (k + 1 < ntiles) blk_next = box_block(k + 1);  // overlap the next lookup
-        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
-          atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
-          *abort_flag = 1;
-          running = false;
-          break;
-        }
-        char* st = smem + s * T::STAGE;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], nvalid * 2u * box_bytes);
-        __syncwarp();
-        if (ok) {
-          const int row = tokb % p.bs;
-          tma_load_4d(st + lane * box_bytes, &kmap, &full[s], 0, g, row, blk);
-          tma_load_4d(st + T::KTILE + lane * box_bytes, &vmap, &full[s], 0, g, row, blk);
-        }
-        if constexpr (TOKS) {
-          float* sks = reinterpret_cast<float*>(st + 2 * T::KTILE);
-          float* svs = sks + T::TT;
-          for (int t = lane; t < T::TT; t += 32) {
-            const int bb = __shfl_sync(kFull, blk, t / box_rows);
-            const int tok = tok0 + t;
-            if (tok < t1 && bb >= 0 && bb < p.nblocks) {
-              const size_t idx = ((size_t)bb * p.bs + tok % p.bs) * p.Hkv + g;
-              cp_async_4(sks + t, p.k_scale + idx);
-              cp_async_4(svs + t, p.v_scale + idx);
-            }
-          }
-          cp_async_arrive_noinc(&full[s]);
-        }
-        ++tile_ctr;
-      }
-    }
-    // Let every copy this warp started land before the CTA may exit.
-    cp_async_wait_all();
-    const uint32_t first = tile_ctr > (uint32_t)T::NSTAGE ? tile_ctr - T::NSTAGE : 0;
-    for (uint32_t j = first; j < tile_ctr; ++j)
-      mbar_wait_drain(&full[j % T::NSTAGE], (j / T::NSTAGE) & 1);
-    return;
+  TileProducer<D, MP, KVK, TOKS> prod;
+  if (warp == 0) {
+    prod.init(&p, &kmap, &vmap, smem, full, empty, qfull, abort_flag, lane, it_begin, it_end);
+    prod.fill(T::NSTAGE - 1);  // every stage starts free
   }
 
-  // -------------------------------------------------------------------- consumers
   const int grp = lane / T::LPT, lg = lane % T::LPT, gbase = lane - lg;
-  const int r_own = lg / T::RSTRIDE;
+  const int v_own = lg / T::RSTRIDE;      // value this lane holds after the scatter
+  const int r_own = v_own % MP;           // its query row
+  const int tk_own = v_own / MP;          // its token of the pair (0 or 1)
+  constexpr int PAIR = MP * T::RSTRIDE;   // lane distance to the same row's other token
   const bool tensor_scale = p.scale_mode == PA_SCALE_PER_TENSOR;
   const float kts = tensor_scale ? __ldg(p.k_scale) : 1.f;
   const float vts = tensor_scale ? __ldg(p.v_scale) : 1.f;
   const float qmul = p.qk_scale * kts;
-  float* mbuf = reinterpret_cast<float*>(smem + T::OFF_MERGE);  // [NCW][MP]
-  float* lbuf = mbuf + T::NCW * MP;                               // [NCW][MP]
-  float* obuf = lbuf + T::NCW * MP;                               // [NCW][MP][D]
-  constexpr int NCT = T::NCW * 32;
-  uint32_t tile_ctr = 0, item_ctr = 0;
+  float* mbuf = reinterpret_cast<float*>(smem + T::OFF_MERGE);  // [NW][MP]
+  float* lbuf = mbuf + T::NW * MP;                                // [NW][MP]
+  uint32_t tile_ctr = 0, items_seen = 0;
 
   int4 item_next = it_begin < it_end ? p.items[it_begin] : make_int4(0, 0, 0, -1);
+  int n_next = 0, ql_next = 0;
+  if (it_begin < it_end) {
+    const int bn = item_next.x / (p.Hkv * p.RB);
+    n_next = __ldg(p.ctx + bn);
+    ql_next = __ldg(p.qlens + bn);
+  }
   for (int it = it_begin; it < it_end; ++it) {
     const int4 item = item_next;
-    if (it + 1 < it_end) item_next = p.items[it + 1];
+    const int n = n_next, ql = ql_next;
+    if (it + 1 < it_end) {
+      item_next = p.items[it + 1];
+      const int bn = item_next.x / (p.Hkv * p.RB);
+      n_next = __ldg(p.ctx + bn);
+      ql_next = __ldg(p.qlens + bn);
+    }
     const int u = item.x, t0 = item.y, t1 = item.z, slot = item.w;
+    if (t1 <= t0) continue;
     const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
-    const int qs = item_ctr & 1;
-    const uint32_t qph = (item_ctr >> 1) & 1;
-    ++item_ctr;
+    const int qs = items_seen % T::NQ;
+    const uint32_t qph = (items_seen / T::NQ) & 1;
+    ++items_seen;
     if (!mbar_wait(&qfull[qs], qph, abort_flag)) {
       atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
       *abort_flag = 1;
     }
+    // query rows as float pairs, pre-scaled by sm_scale * log2(e) (and a per-tensor K scale),
+    // stored in this lane's reduce-scatter order: slot r holds row r ^ r_own
     const char* qslot = smem + T::OFF_Q + qs * T::QSLOT;
-    const int n = *reinterpret_cast<const int*>(qslot + 16);
-    const int ql = *reinterpret_cast<const int*>(qslot + 20);
-    float q[MP][T::DPL];
+    float2 q[MP][T::DPL / 2];
 #pragma unroll
-    for (int r = 0; r < MP; ++r) {
+    for (int rp = 0; rp < MP; ++rp) {
+      const int r = rp ^ r_own;
       const bool row_real = rb * MP + r < p.M;
 #pragma unroll
       for (int c = 0; c < T::CH; ++c) {
         const int ch = lg + c * T::LPT;
-        float f[T::EPC];
-        load_q_elems<QK>(qslot + T::QHDR + (r * D + ch * T::EPC) * 2, T::EPC, f);
 #pragma unroll
-        for (int e = 0; e < T::EPC; ++e) q[r][c * T::EPC + e] = row_real ? f[e] * qmul : 0.f;
+        for (int e = 0; e < T::EPC / 2; ++e) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(qslot + (r * D + ch * T::EPC + 2 * e) * 2);
+          const float2 f = q_pair<QK>(w);
+          q[rp][c * T::EPC / 2 + e] = row_real ? make_float2(f.x * qmul, f.y * qmul)
+                                               : make_float2(0.f, 0.f);
+        }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&qempty[qs]);
-    if (t1 <= t0) continue;
 
     const int rg_own = rb * MP + r_own;
     const int i_own = rg_own / p.G;
     const bool valid_own = rg_own < p.M && i_own < ql;
     const int limit_own = valid_own ? (p.causal ? n - ql + i_own + 1 : n) : 0;
 
-    float m_own = -INFINITY, l_own = 0.f;
-    float o[MP][T::DPL];
+    float m_run = -INFINITY, l_own = 0.f;
+    float2 o[MP][T::DPL / 2];
 #pragma unroll
     for (int r = 0; r < MP; ++r)
 #pragma unroll
-      for (int d = 0; d < T::DPL; ++d) o[r][d] = 0.f;
+      for (int d = 0; d < T::DPL / 2; ++d) o[r][d] = make_float2(0.f, 0.f);
 
     const int ntiles = ceil_div(t1 - t0, T::TT);
+    int s_last = 0;
     for (int k = 0; k < ntiles; ++k) {
+      if (warp == 0) prod.fill(tile_ctr + T::NSTAGE - 1);
       const int s = tile_ctr % T::NSTAGE;
+      s_last = s;
       const uint32_t ph = (tile_ctr / T::NSTAGE) & 1;
       ++tile_ctr;
       if (!mbar_wait(&full[s], ph, abort_flag)) {
@@ -384,70 +662,27 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 1)
       const float* svs = sks + T::TT;
       const int tok0 = t0 + k * T::TT;
       const int n_in = min(T::TT, t1 - tok0);
-      for (int base = warp * T::GPW; base < n_in; base += T::NG) {
-        const int t = base + grp;
-        const bool tv = t < n_in;
-        const int tl = tv ? t : 0;
-        float kf[T::DPL];
-#pragma unroll
-        for (int c = 0; c < T::CH; ++c)
-          load_kv_chunk<KVK, T::EPC>(ks + (size_t)tl * D * T::BPE + (lg + c * T::LPT) * T::CB,
-                                     kf + c * T::EPC);
-        float acc[MP];
-#pragma unroll
-        for (int r = 0; r < MP; ++r) {
-          float a = 0.f;
-#pragma unroll
-          for (int d = 0; d < T::DPL; ++d) a = fmaf(q[r][d], kf[d], a);
-          acc[r] = a;
-        }
-        reduce_scatter<MP, T::LPT / 2>(acc, lane);
-        float sc = acc[0];
-        if constexpr (TOKS) sc *= sks[tl];
-        const int tok = tok0 + t;
-        sc = (tv && tok < limit_own) ? sc : -INFINITY;
-        const bool need = sc > m_own + kRescaleSlack;
-        if (__any_sync(kFull, need)) {
-          const float mn = need ? sc : m_own;
-          const float alpha = (mn == m_own) ? 1.f : fast_exp2(m_own - mn);
-          l_own *= alpha;
-          m_own = mn;
-#pragma unroll
-          for (int r = 0; r < MP; ++r) {
-            const float a = __shfl_sync(kFull, alpha, gbase + r * T::RSTRIDE);
-#pragma unroll
-            for (int d = 0; d < T::DPL; ++d) o[r][d] *= a;
-          }
-        }
-        const float pr = (sc == -INFINITY) ? 0.f : fast_exp2(sc - m_own);
-        l_own += pr;
-        float pv = pr;
-        if constexpr (TOKS) pv *= svs[tl];
-        float pw[MP];
-#pragma unroll
-        for (int r = 0; r < MP; ++r) pw[r] = __shfl_sync(kFull, pv, gbase + r * T::RSTRIDE);
-        if (tv) {
-          float vf[T::DPL];
-#pragma unroll
-          for (int c = 0; c < T::CH; ++c)
-            load_kv_chunk<KVK, T::EPC>(vs + (size_t)t * D * T::BPE + (lg + c * T::LPT) * T::CB,
-                                       vf + c * T::EPC);
-#pragma unroll
-          for (int r = 0; r < MP; ++r)
-#pragma unroll
-            for (int d = 0; d < T::DPL; ++d) o[r][d] = fmaf(pw[r], vf[d], o[r][d]);
-        }
-      }
+      StepCtx<D, MP, KVK, TOKS> cx{ks, vs, sks, svs, tok0, n_in, limit_own, lg, gbase, tk_own};
+      int base = warp * T::GPW * 2;
+      for (; base + 2 * T::GPW <= n_in; base += T::NG * 2)  // every token of the warp step valid
+        token_step<false>(cx, base + 2 * grp, q, o, m_run, l_own);
+      for (; base < n_in; base += T::NG * 2)
+        token_step<true>(cx, base + 2 * grp, q, o, m_run, l_own);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      // without its own merge buffer, the item's last stage holds the merge until it is done
+      if (lane == 0 && (T::OWN_MERGE || k + 1 < ntiles)) mbar_arrive(&empty[s]);
     }
 
     // ---- merge the token groups' states: within the warp, then across warps
+    float* obuf = reinterpret_cast<float*>(
+        smem + (T::OWN_MERGE ? T::OFF_MERGE_O : s_last * T::STAGE));  // [NW][MP][D]
+    __syncwarp();
     float mr[MP], lr[MP];
 #pragma unroll
     for (int r = 0; r < MP; ++r) {
-      mr[r] = __shfl_sync(kFull, m_own, gbase + r * T::RSTRIDE);
-      lr[r] = __shfl_sync(kFull, l_own, gbase + r * T::RSTRIDE);
+      const int la = gbase + r * T::RSTRIDE, lb = la + PAIR;
+      mr[r] = __shfl_sync(kFull, m_run, la);
+      lr[r] = __shfl_sync(kFull, l_own, la) + __shfl_sync(kFull, l_own, lb);
     }
 #pragma unroll
     for (int off = T::LPT; off < 32; off <<= 1) {
@@ -461,9 +696,19 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 1)
         lr[r] = lr[r] * a + lo * bw;
         mr[r] = mn;
 #pragma unroll
-        for (int d = 0; d < T::DPL; ++d)
-          o[r][d] = o[r][d] * a + __shfl_xor_sync(kFull, o[r][d], off) * bw;
+        for (int d = 0; d < T::DPL / 2; ++d) {
+          const float ox = __shfl_xor_sync(kFull, o[r][d].x, off);
+          const float oy = __shfl_xor_sync(kFull, o[r][d].y, off);
+          o[r][d] = make_float2(o[r][d].x * a + ox * bw, o[r][d].y * a + oy * bw);
+        }
       }
+    }
+    if constexpr (!T::OWN_MERGE) {
+      named_barrier_sync(1, T::NTHREADS);  // every warp is done reading the last stage
+    } else {
+      // every warp has released the item's last tile: refill the whole ring before merging,
+      // so the copies keep flowing while the warps combine their states
+      if (warp == 0) prod.fill(tile_ctr + T::NSTAGE - 1);
     }
     if (lane < T::LPT) {
 #pragma unroll
@@ -476,22 +721,23 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 1)
         for (int c = 0; c < T::CH; ++c) {
           const int d0 = (lg + c * T::LPT) * T::EPC;
 #pragma unroll
-          for (int e = 0; e < T::EPC; ++e)
-            obuf[(warp * MP + r) * D + d0 + e] = o[r][c * T::EPC + e];
+          for (int e = 0; e < T::EPC / 2; ++e)
+            *reinterpret_cast<float2*>(&obuf[(warp * MP + r) * D + d0 + 2 * e]) =
+                o[r][c * T::EPC / 2 + e];
         }
       }
     }
-    named_barrier_sync(1, NCT);
-    for (int e = threadIdx.x; e < MP * D; e += NCT) {
+    named_barrier_sync(1, T::NTHREADS);
+    for (int e = threadIdx.x; e < MP * D; e += T::NTHREADS) {
       const int r = e / D, d = e % D, rg = rb * MP + r;
       if (rg >= p.M) continue;
       float mstar = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < T::NCW; ++w) mstar = fmaxf(mstar, mbuf[w * MP + r]);
+      for (int w = 0; w < T::NW; ++w) mstar = fmaxf(mstar, mbuf[w * MP + r]);
       float L = 0.f, O = 0.f;
       if (mstar != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < T::NCW; ++w) {
+        for (int w = 0; w < T::NW; ++w) {
           const float mw = mbuf[w * MP + r];
           const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - mstar);
           L += lbuf[w * MP + r] * wt;
@@ -510,8 +756,27 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 1)
         if (d == 0) p.lse_part[(size_t)slot * MP + r] = lse2;
       }
     }
-    named_barrier_sync(1, NCT);
+    named_barrier_sync(1, T::NTHREADS);
+    if (slot >= 0 && p.merge_in_decode)
+      merge_if_last<D, MP, QK, T::NW>(p, u, b, g, rb, obuf, T::MERGE_O / 4, mbuf, last_flag);
+    if (!T::OWN_MERGE && lane == 0) mbar_arrive(&empty[s_last]);
   }
+  // units with no keys at all: padding rows (zero, lse = -inf), spread over the CTAs
+  if (p.merge_in_decode) {
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      if (__ldg(&p.unit_info[u].y) != 0) continue;
+      const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
+      for (int e = threadIdx.x; e < MP * D; e += T::NTHREADS) {
+        const int r = e / D, d = e % D, rg = rb * MP + r;
+        if (rg >= p.M) continue;
+        const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
+        store_out<QK>(p.out, row * D + d, 0.f);
+        if (d == 0 && p.lse) p.lse[row] = -INFINITY;
+      }
+    }
+  }
+  if (warp == 0) prod.drain();
+  grid_dependents_launch();
 }
 
 template <int D, int MP, int KVK, int QK, bool TOKS>
@@ -525,11 +790,29 @@ cudaError_t launch_simt_instance(const SimtParams& prm, const CUtensorMap& kmap,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, T::NTHREADS, T::SMEM, s>>>(kmap, vmap, prm);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(T::NTHREADS);
+  cfg.dynamicSmemBytes = T::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, prm);
 }
 
 // Dispatch over the row tile and the dtype combination for one head dimension.
+#define PA_SIMT_ROWS(X, MP_)        \
+  X(MP_, KV_BF16, Q_BF16, false)    \
+  X(MP_, KV_FP16, Q_FP16, false)    \
+  X(MP_, KV_FP8, Q_BF16, false)     \
+  X(MP_, KV_FP8, Q_BF16, true)      \
+  X(MP_, KV_FP8, Q_FP16, false)     \
+  X(MP_, KV_FP8, Q_FP16, true)
+#define PA_SIMT_ALL(X) PA_SIMT_ROWS(X, 1) PA_SIMT_ROWS(X, 2) PA_SIMT_ROWS(X, 4) PA_SIMT_ROWS(X, 8)
+
 template <int D>
 cudaError_t launch_simt_for_dim(const SimtParams& prm, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, int grid, int mp, int kvk, int qk,
@@ -537,20 +820,19 @@ cudaError_t launch_simt_for_dim(const SimtParams& prm, const CUtensorMap& kmap,
 #define PA_SIMT_CASE(MP_, KVK_, QK_, TOKS_)                                      \
   if (mp == MP_ && kvk == KVK_ && qk == QK_ && toks == TOKS_)                   \
     return launch_simt_instance<D, MP_, KVK_, QK_, TOKS_>(prm, kmap, vmap, grid, s);
-#define PA_SIMT_ROWS(MP_)                   \
-  PA_SIMT_CASE(MP_, KV_BF16, Q_BF16, false) \
-  PA_SIMT_CASE(MP_, KV_FP16, Q_FP16, false) \
-  PA_SIMT_CASE(MP_, KV_FP8, Q_BF16, false)  \
-  PA_SIMT_CASE(MP_, KV_FP8, Q_BF16, true)   \
-  PA_SIMT_CASE(MP_, KV_FP8, Q_FP16, false)  \
-  PA_SIMT_CASE(MP_, KV_FP8, Q_FP16, true)
-  PA_SIMT_ROWS(1)
-  PA_SIMT_ROWS(2)
-  PA_SIMT_ROWS(4)
-  PA_SIMT_ROWS(8)
-#undef PA_SIMT_ROWS
+  PA_SIMT_ALL(PA_SIMT_CASE)
 #undef PA_SIMT_CASE
   return cudaErrorNotSupported;
+}
+
+// CTAs of one instance that fit on an SM (by shared memory).
+template <int D>
+int simt_ctas_per_sm_for_dim(int mp, int kvk, bool toks) {
+#define PA_SIMT_OCC(MP_, KVK_, QK_, TOKS_) \
+  if (mp == MP_ && kvk == KVK_ && toks == TOKS_) return SimtTraits<D, MP_, KVK_, TOKS_>::CTAS_PER_SM;
+  PA_SIMT_ALL(PA_SIMT_OCC)
+#undef PA_SIMT_OCC
+  return 1;
 }
 
 SimtParams make_simt_params(const DecodeArgs& a);

@@ -9,4 +9,8 @@ cudaError_t launch_simt_d128(const SimtParams& prm, const CUtensorMap& kmap, con
   return launch_simt_for_dim<128>(prm, kmap, vmap, grid, mp, kvk, qk, toks, s);
 }
 
+int simt_ctas_per_sm_d128(int mp, int kvk, bool toks) {
+  return simt_ctas_per_sm_for_dim<128>(mp, kvk, toks);
+}
+
 }  // namespace pa

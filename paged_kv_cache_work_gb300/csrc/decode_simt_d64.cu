@@ -9,4 +9,8 @@ cudaError_t launch_simt_d64(const SimtParams& prm, const CUtensorMap& kmap, cons
   return launch_simt_for_dim<64>(prm, kmap, vmap, grid, mp, kvk, qk, toks, s);
 }
 
+int simt_ctas_per_sm_d64(int mp, int kvk, bool toks) {
+  return simt_ctas_per_sm_for_dim<64>(mp, kvk, toks);
+}
+
 }  // namespace pa

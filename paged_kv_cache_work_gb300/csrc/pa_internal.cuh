@@ -27,13 +27,14 @@ __host__ __device__ constexpr size_t round_up_sz(size_t a, size_t b) { return (a
 // tiles of `mp` (a power of two); a unit of work is one (sequence, kv head, row
 // tile), and `tt` is the number of tokens staged per pipeline stage.
 struct Variant {
-  int rows;    // M = G * Sq
-  int mp;      // rows per unit (padded to a power of two)
-  int rb;      // row tiles per kv head
-  int tt;      // tokens per stage (tile)
-  int units;   // B * Hkv * rb
-  int ctas;    // persistent grid size C
-  int bpe;     // bytes per cache element
+  int rows;         // M = G * Sq
+  int mp;           // rows per unit (padded to a power of two)
+  int rb;           // row tiles per kv head
+  int tt;           // tokens per stage (tile)
+  int units;        // B * Hkv * rb
+  int ctas;         // persistent grid size C
+  int ctas_per_sm;  // decode CTAs resident per SM
+  int bpe;          // bytes per cache element
 };
 
 // Largest row tile of the CUDA-core decode kernel.
@@ -47,7 +48,11 @@ inline int pow2_at_least(int x) {
   return p;
 }
 
-inline Variant make_variant(const pa_config& c, int ctas) {
+// CTAs of the CUDA-core decode instance for these parameters that fit on one SM.
+int simt_ctas_per_sm(int head_dim, int mp, int kvk, bool toks);
+
+// Everything but the grid size, which needs the device (see api.cu).
+inline Variant make_variant(const pa_config& c) {
   Variant v{};
   v.rows = (c.num_q_heads / c.num_kv_heads) * c.max_q_len;
   v.mp = v.rows <= kSimtMaxRows ? pow2_at_least(v.rows) : kSimtMaxRows;
@@ -55,7 +60,9 @@ inline Variant make_variant(const pa_config& c, int ctas) {
   v.bpe = c.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
   v.tt = kTileBytes / (c.head_dim * v.bpe);
   v.units = c.batch * c.num_kv_heads * v.rb;
-  v.ctas = ctas;
+  const int kvk = c.kv_dtype == PA_FP8_E4M3 ? 2 : (c.kv_dtype == PA_FP16 ? 1 : 0);
+  v.ctas_per_sm = simt_ctas_per_sm(c.head_dim, v.mp, kvk, c.kv_scale_mode == PA_SCALE_PER_TOKEN);
+  v.ctas = 0;
   return v;
 }
 
@@ -64,12 +71,15 @@ inline Variant make_variant(const pa_config& c, int ctas) {
 //   header     int32[64]: [0] flags, [1] chunk, [2] active CTAs, [3] items
 //   item_off   int32[C + 1]      first work item of each CTA
 //   items      int4[C + units]   (unit, t0, t1, partial slot or -1)
-//   unit_info  int2[units]       (first partial slot, number of splits)
-//   unit_start int32[units + 1]  start of each unit in the concatenated token space
-//   o_part     f32[(C + units) * mp * D]   normalised partial outputs
-//   lse_part   f32[(C + units) * mp]       their log2-sum-exp
+//   unit_info  int2[units]       (slot of the first piece, number of pieces); piece s > 0
+//                                of a unit sits in slot 2 * (first / 2 + s)
+//   unit_cnt   int32[units]      pieces of each unit finished so far (merge in decode)
+//   seq_start  int32[B + 1]      planner scratch for very large batches
+//   seq_len    int32[B]
+//   o_part     f32[2C * mp * D]  normalised partial outputs (CTA c: slots 2c, 2c + 1)
+//   lse_part   f32[2C * mp]      their log2-sum-exp
 struct WsLayout {
-  size_t header, item_off, items, unit_info, unit_start, o_part, lse_part, total;
+  size_t header, item_off, items, unit_info, unit_cnt, seq_start, seq_len, o_part, lse_part, total;
 };
 
 inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
@@ -85,14 +95,48 @@ inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
   L.item_off = take(((size_t)v.ctas + 1) * sizeof(int32_t));
   L.items = take(max_items * sizeof(int4));
   L.unit_info = take((size_t)v.units * sizeof(int2));
-  L.unit_start = take(((size_t)v.units + 1) * sizeof(int32_t));
-  L.o_part = take(max_items * (size_t)v.mp * c.head_dim * sizeof(float));
-  L.lse_part = take(max_items * (size_t)v.mp * sizeof(float));
+  L.unit_cnt = take((size_t)v.units * sizeof(int32_t));
+  L.seq_start = take(((size_t)c.batch + 1) * sizeof(int32_t));
+  L.seq_len = take((size_t)c.batch * sizeof(int32_t));
+  const size_t slots = 2 * (size_t)v.ctas;
+  L.o_part = take(slots * (size_t)v.mp * c.head_dim * sizeof(float));
+  L.lse_part = take(slots * (size_t)v.mp * sizeof(float));
   L.total = off;
   return L;
 }
 
 enum HeaderSlot { HDR_FLAGS = 0, HDR_CHUNK = 1, HDR_ACTIVE = 2, HDR_ITEMS = 3 };
+
+// Division by a run-time constant d in [1, 2^31) of a dividend n in [0, 2^31) with one
+// multiply-high, add and shift (the round-up multiplier method of Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994): with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1, n / d = (mulhi(n, m) + n) >> s.
+struct FastDiv {
+  uint32_t d, m, s;
+  __host__ __device__ FastDiv() : d(1), m(1), s(0) {}
+  __host__ __device__ explicit FastDiv(uint32_t div) : d(div) {
+    s = 0;
+    while ((1u << s) < d) ++s;
+    m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << s) - d)) / d) + 1;
+  }
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+#if defined(__CUDA_ARCH__)
+    const uint32_t hi = __umulhi(n, m);
+#else
+    const uint32_t hi = (uint32_t)(((uint64_t)n * m) >> 32);
+#endif
+    return (hi + n) >> s;
+  }
+  __host__ __device__ __forceinline__ uint32_t mod(uint32_t n) const { return n - div(n) * d; }
+};
+
+// log2 of a power of two.
+__host__ __device__ constexpr int ilog2(uint32_t x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
+
+// Partial slot of piece s of a unit whose first piece sits in slot `first`.
+__host__ __device__ inline int piece_slot(int first, int s) {
+  return s == 0 ? first : 2 * ((first >> 1) + s);
+}
 
 // Launch helpers implemented in plan.cu / decode_*.cu / reduce.cu.
 struct ProblemArgs {
@@ -121,6 +165,7 @@ struct DecodeArgs {
   WsLayout L;
   Variant v;
   int q_kind, kv_kind;
+  int merge_in_decode;
 };
 
 // Returns cudaErrorNotSupported when no kernel instance matches.
@@ -247,6 +292,25 @@ __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32x2 multiply-add (sm_100 family): d = a * b + c, lane-wise on float2.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
+// Programmatic dependent launch: wait until the preceding kernel in the stream has
+// completed and its writes are visible / let the following kernel start launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Named barrier over the first `count` threads of the CTA (id 1; id 0 is __syncthreads).

@@ -3,35 +3,44 @@
 // The split follows "Optimize paged-attention metadata decode" (FlyDSL PR #910, Summary and
 // Changes): metadata is generated on the device for a persistent decode grid sized as SMs x
 // a grid multiplier (default 1, the safe one-grid-per-CU choice), and ranges that a unit
-// does not finish in one piece are merged by a separate reducer.  Here every unit
-// (sequence, kv head, row tile) contributes its context length, rounded up to whole tiles,
-// to one concatenated token space; that space is cut into C equal tile-aligned pieces, one
-// per CTA, so every CTA streams the same number of KV bytes.  A piece that crosses unit
+// does not finish in one piece are merged by a split reducer.  Here every unit (sequence,
+// kv head, row tile) contributes its context length, rounded up to whole tiles, to one
+// concatenated token space; that space is cut into C equal tile-aligned pieces, one per
+// CTA, so every CTA streams the same number of KV bytes.  A piece that crosses unit
 // boundaries becomes several work items, processed by its CTA in order.
 //
-// One CTA of 1024 threads does everything with block-wide scans; it also checks the
-// lengths and every block id in use and, on any problem, emits an empty work list so the
-// decode kernel touches nothing (the flags word records why).
+// Only the first and the last item of a piece can be part of a unit cut into several
+// pieces, so CTA c writes at most two partial results, in slots 2c (its first item) and
+// 2c + 1 (its last): the slots of a unit follow from the first CTA it appears in, with no
+// prefix sum over units.  All units of a sequence have the same length, so the planner works
+// on per-sequence prefix sums in shared memory.  One CTA does everything; it checks the
+// lengths and, on a bad one, emits an empty work list so the decode kernel touches nothing
+// (the flags word records why).  Block ids are checked by the decode kernel as it reads them.
 #include "pa_internal.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 512;
+constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kPlanSmemSeqs = 4096;  // sequences whose prefix sums fit in shared memory
 
 struct PlanParams {
-  const int32_t* bt;
   const int32_t* ctx;
   const int32_t* qlens;
   int32_t* hdr;
   int32_t* item_off;
   int4* items;
   int2* unit_info;
-  int32_t* unit_start;
-  int batch, max_q_len, num_kv_heads, rb, block_size, max_blocks, num_blocks, tt, ctas, units;
+  int32_t* unit_cnt;
+  int32_t* seq_start_g;  // B + 1 ints in the workspace, used when B > kPlanSmemSeqs
+  int32_t* seq_len_g;    // B ints
+  int batch, max_q_len, num_kv_heads, rb, block_size, max_blocks, tt, ctas, units;
+  int tt_shift;    // log2(tt): tiles are a power of two
+  FastDiv ups_div; // units per sequence
 };
 
-// Exclusive prefix sum of one value per thread over the 1024-thread block.
+// Exclusive prefix sum of one value per thread over the block.
 __device__ int block_exclusive_scan(int v, int* total, int* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -43,25 +52,25 @@ __device__ int block_exclusive_scan(int v, int* total, int* sh) {
   if (lane == 31) sh[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = sh[lane];
+    int w = lane < kPlanWarps ? sh[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(kFull, w, o);
       if (lane >= o) w += y;
     }
-    sh[lane] = w;
+    if (lane < kPlanWarps) sh[lane] = w;
   }
   __syncthreads();
   const int excl = x - v + (warp > 0 ? sh[warp - 1] : 0);
-  *total = sh[31];
+  *total = sh[kPlanWarps - 1];
   __syncthreads();
   return excl;
 }
 
-// Last unit whose start is <= x (units of zero length share their successor's start and
-// are skipped by taking the last such index).
-__device__ int find_unit(const int32_t* start, int units, int x) {
-  int lo = 0, hi = units;  // start[units] > x for every x inside the token space
+// Last sequence whose start is <= x (sequences with no tokens share their successor's
+// start and are skipped by taking the last such index).
+__device__ int find_seq(const int32_t* start, int batch, int x) {
+  int lo = 0, hi = batch;  // start[batch] > x for every x inside the token space
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
     if (start[mid] <= x)
@@ -75,69 +84,78 @@ __device__ int find_unit(const int32_t* start, int units, int x) {
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams p) {
   __shared__ int sh[32];
   __shared__ int s_flags;
+  __shared__ int32_t s_start[kPlanSmemSeqs + 1];
+  __shared__ int32_t s_len[kPlanSmemSeqs];
+  __shared__ uint32_t s_chunk_div[3];  // FastDiv of the chunk: d, m, s
+  grid_dependency_wait();     // lengths may come from the previous kernel in the stream
+  grid_dependents_launch();   // the decode grid can stage its prologue meanwhile
   const int tid = threadIdx.x;
+  const bool in_smem = p.batch <= kPlanSmemSeqs;
+  int32_t* seq_start = in_smem ? s_start : p.seq_start_g;
+  int32_t* seq_len = in_smem ? s_len : p.seq_len_g;
   if (tid == 0) s_flags = 0;
   __syncthreads();
 
   // 1. lengths
   for (int b = tid; b < p.batch; b += kPlanThreads) {
-    const int n = p.ctx[b], ql = p.qlens[b];
+    const int n = __ldg(p.ctx + b), ql = __ldg(p.qlens + b);
     const long long cap = (long long)p.max_blocks * p.block_size;
-    if (ql < 0 || ql > p.max_q_len || n < ql || (long long)n > cap)
-      atomicOr(&s_flags, PA_FLAG_BAD_LENGTHS);
-  }
-  __syncthreads();
-  // 2. block ids of every page in use (only once the lengths are known to be sane)
-  if (s_flags == 0) {
-    const long long total = (long long)p.batch * p.max_blocks;
-    for (long long idx = tid; idx < total; idx += kPlanThreads) {
-      const int b = (int)(idx / p.max_blocks), pg = (int)(idx % p.max_blocks);
-      const int pages = (p.ctx[b] + p.block_size - 1) / p.block_size;
-      if (pg < pages) {
-        const int id = p.bt[idx];
-        if (id < 0 || id >= p.num_blocks) atomicOr(&s_flags, PA_FLAG_BAD_BLOCK_ID);
-      }
-    }
+    const bool bad = ql < 0 || ql > p.max_q_len || n < ql || (long long)n > cap;
+    if (bad) atomicOr(&s_flags, PA_FLAG_BAD_LENGTHS);
+    seq_len[b] = n;
   }
   __syncthreads();
   const int flags = s_flags;
-  const int per_seq = p.num_kv_heads * p.rb;
+  const int ups = p.num_kv_heads * p.rb;  // units per sequence
+  auto pad = [&](int len) { return ((len + p.tt - 1) >> p.tt_shift) << p.tt_shift; };
 
-  // 3. unit starts in the concatenated, tile-padded token space
+  // 2. start of each sequence's units in the concatenated, tile-padded token space
   int carry = 0, tot = 0;
-  for (int base = 0; base < p.units; base += kPlanThreads) {
-    const int u = base + tid;
+  for (int base = 0; base < p.batch; base += kPlanThreads) {
+    const int b = base + tid;
     int len = 0;
-    if (u < p.units && flags == 0) len = round_up(p.ctx[u / per_seq], p.tt);
+    if (b < p.batch && flags == 0) len = pad(seq_len[b]) * ups;
     const int excl = block_exclusive_scan(len, &tot, sh);
-    if (u < p.units) p.unit_start[u] = carry + excl;
+    if (b < p.batch) seq_start[b] = carry + excl;
     carry += tot;
   }
   const int T = carry;
-  if (tid == 0) p.unit_start[p.units] = T;
+  if (tid == 0) seq_start[p.batch] = T;
   __syncthreads();
 
-  // 4. equal tile-aligned pieces, one per CTA
-  const int chunk = T > 0 ? round_up(ceil_div(T, p.ctas), p.tt) : p.tt;
+  // 3. equal tile-aligned pieces, one per CTA
+  const int chunk = T > 0 ? pad(ceil_div(T, p.ctas)) : p.tt;
   const int active = T > 0 ? ceil_div(T, chunk) : 0;
-
-  // 5. splits per unit and the first partial slot of units done in several pieces
-  carry = 0;
-  for (int base = 0; base < p.units; base += kPlanThreads) {
-    const int u = base + tid;
-    int ns = 0;
-    if (u < p.units) {
-      const int st = p.unit_start[u], en = p.unit_start[u + 1];
-      if (en > st) ns = (en - 1) / chunk - st / chunk + 1;
-    }
-    const int parts = ns >= 2 ? ns : 0;
-    const int excl = block_exclusive_scan(parts, &tot, sh);
-    if (u < p.units) p.unit_info[u] = make_int2(carry + excl, ns);
-    carry += tot;
+  if (tid == 0) {
+    const FastDiv f((uint32_t)chunk);
+    s_chunk_div[0] = f.d;
+    s_chunk_div[1] = f.m;
+    s_chunk_div[2] = f.s;
   }
   __syncthreads();
+  FastDiv cdiv;
+  cdiv.d = s_chunk_div[0];
+  cdiv.m = s_chunk_div[1];
+  cdiv.s = s_chunk_div[2];
 
-  // 6. work items, CTA by CTA
+  // 4. per unit: its pieces and the slot of its first partial (independent per unit)
+  for (int u = tid; u < p.units; u += kPlanThreads) {
+    int ns = 0, first = 0;
+    if (flags == 0) {
+      const int b = p.ups_div.div(u), k = u - b * ups;
+      const int plen = pad(seq_len[b]);
+      const int st = seq_start[b] + k * plen;
+      if (plen > 0) {
+        const int c0 = cdiv.div(st);
+        ns = cdiv.div(st + plen - 1) - c0 + 1;
+        first = 2 * c0 + (c0 * chunk < st ? 1 : 0);  // the last item of CTA c0, or its first
+      }
+    }
+    p.unit_info[u] = make_int2(first, ns);
+    p.unit_cnt[u] = 0;
+  }
+
+  // 5. work items, CTA by CTA
   carry = 0;
   for (int base = 0; base < p.ctas; base += kPlanThreads) {
     const int c = base + tid;
@@ -145,22 +163,26 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     if (c < active) {
       lo = c * chunk;
       hi = min(lo + chunk, T) - 1;
-      uf = find_unit(p.unit_start, p.units, lo);
-      cnt = find_unit(p.unit_start, p.units, hi) - uf + 1;
+      const int bf = find_seq(seq_start, p.batch, lo), bl = find_seq(seq_start, p.batch, hi);
+      const int pf = pad(seq_len[bf]), pl = pad(seq_len[bl]);
+      uf = bf * ups + (lo - seq_start[bf]) / pf;
+      const int ul = bl * ups + (hi - seq_start[bl]) / pl;
+      cnt = ul - uf + 1;
     }
     const int excl = block_exclusive_scan(cnt, &tot, sh);
     if (c < p.ctas) p.item_off[c] = carry + excl;
     for (int k = 0; k < cnt; ++k) {
       const int u = uf + k;
-      const int st = p.unit_start[u], en = p.unit_start[u + 1];
-      int t0 = 0, t1 = 0;
-      if (en > st) {
-        const int len = p.ctx[u / per_seq];
+      const int b = p.ups_div.div(u), ku = u - b * ups;
+      const int len = seq_len[b];
+      const int plen = pad(len);
+      const int st = seq_start[b] + ku * plen;
+      int t0 = 0, t1 = 0, slot = -1;
+      if (plen > 0) {
         t0 = max(lo, st) - st;
         t1 = min(hi + 1 - st, len);
+        if (cdiv.div(st + plen - 1) != cdiv.div(st)) slot = 2 * c + (k > 0 ? 1 : 0);
       }
-      const int2 info = p.unit_info[u];
-      const int slot = info.y >= 2 ? info.x + (c - st / chunk) : -1;
       p.items[carry + excl + k] = make_int4(u, t0, t1, slot);
     }
     carry += tot;
@@ -179,26 +201,36 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
 cudaError_t launch_plan(const ProblemArgs& a, const Variant& v, const WsLayout& L, char* ws,
                         cudaStream_t s) {
   PlanParams p;
-  p.bt = a.block_tables;
   p.ctx = a.context_lens;
   p.qlens = a.q_lens;
   p.hdr = reinterpret_cast<int32_t*>(ws + L.header);
   p.item_off = reinterpret_cast<int32_t*>(ws + L.item_off);
   p.items = reinterpret_cast<int4*>(ws + L.items);
   p.unit_info = reinterpret_cast<int2*>(ws + L.unit_info);
-  p.unit_start = reinterpret_cast<int32_t*>(ws + L.unit_start);
+  p.unit_cnt = reinterpret_cast<int32_t*>(ws + L.unit_cnt);
+  p.seq_start_g = reinterpret_cast<int32_t*>(ws + L.seq_start);
+  p.seq_len_g = reinterpret_cast<int32_t*>(ws + L.seq_len);
   p.batch = a.batch;
   p.max_q_len = a.max_q_len;
   p.num_kv_heads = a.num_kv_heads;
   p.rb = v.rb;
   p.block_size = a.block_size;
   p.max_blocks = a.max_blocks;
-  p.num_blocks = a.num_blocks;
   p.tt = v.tt;
   p.ctas = v.ctas;
   p.units = v.units;
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  p.tt_shift = ilog2((uint32_t)v.tt);
+  p.ups_div = FastDiv((uint32_t)(a.num_kv_heads * v.rb));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, p);
 }
 
 }  // namespace pa

@@ -6,8 +6,8 @@
 // reducer" that follows the persistent decode in "Optimize paged-attention metadata
 // decode" (FlyDSL PR #910, Summary and Performance: metadata decode plus split reducer).
 // Units the decode finished in one piece are skipped; units with no keys at all (a
-// sequence with no context) get zero rows and lse = -inf.  The sum over splits runs in a
-// fixed order, so repeated calls are bitwise identical.
+// sequence with no context) get zero rows and lse = -inf.  Sums over splits run in a fixed
+// order (lane-strided, then a fixed shuffle tree), so repeated calls are bitwise identical.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -17,6 +17,17 @@ namespace pa {
 
 cudaError_t launch_simt_d64(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                             int, int, bool, cudaStream_t);
+int simt_ctas_per_sm_d64(int, int, bool);
+int simt_ctas_per_sm_d128(int, int, bool);
+int simt_ctas_per_sm_d256(int, int, bool);
+
+int simt_ctas_per_sm(int head_dim, int mp, int kvk, bool toks) {
+  switch (head_dim) {
+    case 64: return simt_ctas_per_sm_d64(mp, kvk, toks);
+    case 128: return simt_ctas_per_sm_d128(mp, kvk, toks);
+    default: return simt_ctas_per_sm_d256(mp, kvk, toks);
+  }
+}
 cudaError_t launch_simt_d128(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                              int, int, bool, cudaStream_t);
 cudaError_t launch_simt_d256(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
@@ -37,6 +48,10 @@ SimtParams make_simt_params(const DecodeArgs& a) {
   p.o_part = reinterpret_cast<float*>(a.ws + a.L.o_part);
   p.lse_part = reinterpret_cast<float*>(a.ws + a.L.lse_part);
   p.flags = reinterpret_cast<int32_t*>(a.ws + a.L.header) + HDR_FLAGS;
+  p.unit_info = reinterpret_cast<const int2*>(a.ws + a.L.unit_info);
+  p.unit_cnt = reinterpret_cast<int32_t*>(a.ws + a.L.unit_cnt);
+  p.units = a.v.units;
+  p.merge_in_decode = a.merge_in_decode;
   p.scale_mode = a.scale_mode;
   p.Sq = a.p.max_q_len;
   p.Hq = a.p.num_q_heads;
@@ -45,6 +60,7 @@ SimtParams make_simt_params(const DecodeArgs& a) {
   p.M = a.v.rows;
   p.RB = a.v.rb;
   p.bs = a.p.block_size;
+  p.bs_shift = ilog2((uint32_t)a.p.block_size);
   p.maxb = a.p.max_blocks;
   p.nblocks = a.p.num_blocks;
   p.causal = a.p.causal;
@@ -76,39 +92,58 @@ struct ReduceParams {
   int q_kind;
 };
 
-__global__ void __launch_bounds__(256) reduce_kernel(const ReduceParams p) {
+constexpr int kReduceWarps = 4;
+
+// One CTA per unit; warp w merges rows w, w + 4, ...: the lanes share the splits for the
+// max and the weight sum, then the head dimensions for the weighted sum of the partials.
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p) {
+  grid_dependency_wait();  // partials come from the decode kernel launched just before
   const int u = blockIdx.x;
   const int2 info = p.unit_info[u];
-  if (info.y == 1) return;  // written by the decode kernel
-  const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
-  for (int e = threadIdx.x; e < p.MP * p.D; e += blockDim.x) {
-    const int r = e / p.D, d = e % p.D, rg = rb * p.MP + r;
-    if (rg >= p.M) continue;
-    float val = 0.f, lse2 = -INFINITY;
-    if (info.y >= 2) {
+  if (info.y != 1) {
+    const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r = warp; r < p.MP; r += kReduceWarps) {
+      const int rg = rb * p.MP + r;
+      if (rg >= p.M) continue;
+      const int i = rg / p.G, h = g * p.G + rg % p.G;
+      const size_t row = ((size_t)b * p.Sq + i) * p.Hq + h;
       float m = -INFINITY;
-      for (int s = 0; s < info.y; ++s) m = fmaxf(m, p.lse_part[(size_t)(info.x + s) * p.MP + r]);
+      for (int s = lane; s < info.y; s += 32)
+        m = fmaxf(m, p.lse_part[(size_t)piece_slot(info.x, s) * p.MP + r]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      float W = 0.f;
       if (m != -INFINITY) {
-        float W = 0.f, O = 0.f;
-        for (int s = 0; s < info.y; ++s) {
-          const size_t part = (size_t)(info.x + s) * p.MP + r;
-          const float ls = p.lse_part[part];
-          const float w = ls == -INFINITY ? 0.f : fast_exp2(ls - m);
-          W += w;
-          O += w * p.o_part[part * p.D + d];
+        for (int s = lane; s < info.y; s += 32) {
+          const float ls = p.lse_part[(size_t)piece_slot(info.x, s) * p.MP + r];
+          W += ls == -INFINITY ? 0.f : fast_exp2(ls - m);
         }
-        val = O / W;
-        lse2 = m + fast_log2(W);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
       }
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      for (int d = lane; d < p.D; d += 32) {
+        float O = 0.f;
+        if (W > 0.f) {
+#pragma unroll 4
+          for (int s = 0; s < info.y; ++s) {
+            const size_t part = (size_t)piece_slot(info.x, s) * p.MP + r;
+            const float ls = p.lse_part[part];
+            const float w = ls == -INFINITY ? 0.f : fast_exp2(ls - m);
+            O += w * p.o_part[part * p.D + d];
+          }
+        }
+        const float val = O * inv;
+        if (p.q_kind == Q_BF16)
+          reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.D + d] = __float2bfloat16_rn(val);
+        else
+          reinterpret_cast<__half*>(p.out)[row * p.D + d] = __float2half_rn(val);
+      }
+      if (lane == 0 && p.lse) p.lse[row] = W > 0.f ? (m + fast_log2(W)) * kLn2 : -INFINITY;
     }
-    const int i = rg / p.G, h = g * p.G + rg % p.G;
-    const size_t row = ((size_t)b * p.Sq + i) * p.Hq + h;
-    if (p.q_kind == Q_BF16)
-      reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.D + d] = __float2bfloat16_rn(val);
-    else
-      reinterpret_cast<__half*>(p.out)[row * p.D + d] = __float2half_rn(val);
-    if (d == 0 && p.lse) p.lse[row] = lse2 * kLn2;
   }
+  grid_dependents_launch();
 }
 
 }  // namespace
@@ -130,8 +165,16 @@ cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s) {
   p.D = a.p.head_dim;
   p.q_kind = a.q_kind;
   if (a.v.units == 0) return cudaSuccess;
-  reduce_kernel<<<a.v.units, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.v.units);
+  cfg.blockDim = dim3(kReduceWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reduce_kernel, p);
 }
 
 }  // namespace pa

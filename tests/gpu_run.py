@@ -16,8 +16,9 @@ FP8_ATOL = 3e-2
 LSE_TOL = 2e-4
 
 
-def run(inp_dev: dict, num_ctas: int = 0, grid_mult: int = 0, with_lse: bool = True):
-    cfg = pa.config_for(inp_dev, num_ctas=num_ctas, grid_mult=grid_mult)
+def run(inp_dev: dict, num_ctas: int = 0, grid_mult: int = 0, with_lse: bool = True,
+        split_merge: int = pa.MERGE_IN_DECODE):
+    cfg = pa.config_for(inp_dev, num_ctas=num_ctas, grid_mult=grid_mult, split_merge=split_merge)
     q = inp_dev["q"]
     out = torch.full_like(q, float("nan"))
     lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=q.device) \
@@ -91,9 +92,11 @@ def layout(cfg: pa.PaConfig, v: dict):
     take("item_off", (C + 1) * 4)
     take("items", (C + U) * 16)
     take("unit_info", U * 8)
-    take("unit_start", (U + 1) * 4)
-    take("o_part", (C + U) * v["mp"] * cfg.head_dim * 4)
-    take("lse_part", (C + U) * v["mp"] * 4)
+    take("unit_cnt", U * 4)
+    take("seq_start", (cfg.batch + 1) * 4)
+    take("seq_len", cfg.batch * 4)
+    take("o_part", 2 * C * v["mp"] * cfg.head_dim * 4)
+    take("lse_part", 2 * C * v["mp"] * 4)
     out["total"] = off
     return out
 
@@ -113,9 +116,9 @@ def plan_view(ws: torch.Tensor, cfg: pa.PaConfig, ctas: int):
     item_off = arr("item_off", np.int32, C + 1)
     items = arr("items", np.int32, 4 * (C + U)).reshape(-1, 4)
     unit_info = arr("unit_info", np.int32, 2 * U).reshape(-1, 2)
-    o_part = arr("o_part", np.float32, (C + U) * v["mp"] * cfg.head_dim).reshape(
-        C + U, v["mp"], cfg.head_dim)
-    lse_part = arr("lse_part", np.float32, (C + U) * v["mp"]).reshape(C + U, v["mp"])
+    o_part = arr("o_part", np.float32, 2 * C * v["mp"] * cfg.head_dim).reshape(
+        2 * C, v["mp"], cfg.head_dim)
+    lse_part = arr("lse_part", np.float32, 2 * C * v["mp"]).reshape(2 * C, v["mp"])
     return dict(v=v, flags=int(hdr[0]), chunk=int(hdr[1]), active=int(hdr[2]),
                 n_items=int(hdr[3]), item_off=item_off.copy(), items=items.copy(),
                 unit_info=unit_info.copy(), o_part=o_part.copy(), lse_part=lse_part.copy())

@@ -161,3 +161,29 @@ def test_without_lse_output(cuda_device, pa):
     ref_out, _ = oracle.decode(inp, "f32")
     out, _, _, _ = run(W.to_device(inp, cuda_device), with_lse=False)
     compare(out, None, ref_out, None, "bf16")
+
+
+MERGE_CASES = [W.reduced(W.GQA_B32, 5, 300, 1400), W.reduced(W.LONG_SQ4, 2, 2500, 6000),
+               W.reduced(W.FP8_TOKEN_SQ4, 3, 1100, 3000), W.reduced(W.mha_d256(8, 16), 2, 200, 1300)]
+
+
+@pytest.mark.parametrize("ctas", [0, 40])
+@pytest.mark.parametrize("wl", MERGE_CASES, ids=lambda w: w.name)
+def test_split_merge_in_reduce_kernel(wl, ctas, cuda_device, pa):
+    """The standalone reducer (PA_MERGE_IN_REDUCE) against the oracle."""
+    inp = W.make_inputs(wl, 2039)
+    ref_out, ref_lse = oracle.decode(inp, "f32")
+    out, lse, ws, _ = run(W.to_device(inp, cuda_device), num_ctas=ctas,
+                          split_merge=pa.MERGE_IN_REDUCE)
+    compare(out, lse, ref_out, ref_lse, wl.kv_dtype)
+    assert pa.read_flags(ws) == 0
+
+
+def test_empty_sequences_with_reduce_kernel(cuda_device, pa):
+    rng = np.random.default_rng(5)
+    inp, _ = random_problem(rng, batch=4, max_q_len=2, num_q_heads=4, num_kv_heads=2,
+                            head_dim=128, block_size=16, ctx=[0, 90, 0, 33], q_lens=[0, 2, 0, 1],
+                            causal=True)
+    ref_out, ref_lse = oracle.decode(inp, "f32")
+    out, lse, _, _ = run(W.to_device(inp, cuda_device), num_ctas=7, split_merge=pa.MERGE_IN_REDUCE)
+    compare(out, lse, ref_out, ref_lse, "bf16")

@@ -5,7 +5,8 @@
 * every CTA's piece is contiguous in the concatenated tile-padded token space and no
   longer than the chunk, and the chunk is the smallest tile multiple that fits the work
   in C pieces;
-* the partial slots of units cut into several pieces are distinct and dense;
+* the partial slots of units cut into several pieces are CTA c's slots 2c / 2c + 1, and
+  the unit table points at them;
 * each partial the decode kernel wrote equals the oracle's attention over that item's
   key range (so the split mode is checked on its own, before the reducer).
 """
@@ -46,7 +47,8 @@ def check_plan(view, ctx, ctas, hkv):
         lo = c * chunk
         hi = min(lo + chunk, T) if active else lo
         pos = lo
-        for it in range(item_off[c], item_off[c + 1]):
+        n_c = item_off[c + 1] - item_off[c]
+        for k, it in enumerate(range(item_off[c], item_off[c + 1])):
             u, t0, t1, slot = (int(x) for x in items[it])
             assert active and 0 <= u < U
             if t1 <= t0:
@@ -61,6 +63,9 @@ def check_plan(view, ctx, ctas, hkv):
                 pos = start[u] + plen[u]
             covered[u][t0:t1] += 1
             slots.setdefault(u, []).append(slot)
+            if slot >= 0:  # only a piece's first or last item can be split
+                assert slot == 2 * c + (1 if k > 0 else 0)
+                assert k == 0 or k == n_c - 1
         assert pos == hi, "piece does not end where the next begins"
     for u in range(U):
         assert (covered[u] == 1).all(), f"unit {u} not covered exactly once"
@@ -70,7 +75,8 @@ def check_plan(view, ctx, ctas, hkv):
         if ns == 1:
             assert slots[u] == [-1]
         elif ns > 1:
-            assert slots[u] == list(range(int(info[0]), int(info[0]) + ns))
+            first = int(info[0])
+            assert slots[u] == [first] + [2 * (first // 2 + s) for s in range(1, ns)]
     return T
 
 

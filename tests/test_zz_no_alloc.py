@@ -57,8 +57,9 @@ def test_static_step_refuses_problems_beyond_its_scratch(cuda_device):
     lib = pa.load()
     inp = W.make_inputs(W.reduced(W.GQA_B32, 2, 16, 64), 2026, device=cuda_device)
     cfg = pa.config_for(inp)
-    cfg.batch = 4096  # work list and partials for 4096 sequences exceed the static array
-    assert pa.workspace_size(cfg) > pa.STATIC_SCRATCH_BYTES
+    while pa.workspace_size(cfg) <= pa.STATIC_SCRATCH_BYTES:
+        cfg.batch *= 2  # the work list grows with the batch until it no longer fits
+    assert cfg.batch > inp["workload"].batch
     out = torch.empty(1, device=cuda_device)
     lse = torch.empty(1, device=cuda_device)
     assert _static_call(lib, cfg, inp, out, lse) == pa.ERR_WORKSPACE
