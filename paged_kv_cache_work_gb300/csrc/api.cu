@@ -119,8 +119,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Descriptor of a cache [num_blocks, block_size, Hkv, D] seen as a 4-D tensor (D innermost)
-// with a box of one head's rows of one page: {D, 1, rows, 1}.
-bool kv_tensor_map(CUtensorMap* m, const void* base, const pa_config& c, int box_rows) {
+// with a box of one head's rows of one page.  CUDA-core kernel: {D, 1, rows, 1}, no swizzle.
+// Tensor-core kernel: {128 bytes of D, 1, rows, 1} with the 128-byte swizzle, one box per
+// 128-byte column slab.
+bool kv_tensor_map(CUtensorMap* m, const void* base, const pa_config& c, int box_rows, bool slabs) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const int bpe = c.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
@@ -132,11 +134,13 @@ bool kv_tensor_map(CUtensorMap* m, const void* base, const pa_config& c, int box
   cuuint64_t strides[3] = {(cuuint64_t)c.head_dim * bpe,
                            (cuuint64_t)c.num_kv_heads * c.head_dim * bpe,
                            (cuuint64_t)c.block_size * c.num_kv_heads * c.head_dim * bpe};
-  cuuint32_t box[4] = {(cuuint32_t)c.head_dim, 1, (cuuint32_t)box_rows, 1};
+  const cuuint32_t inner = slabs ? (cuuint32_t)(128 / bpe) : (cuuint32_t)c.head_dim;
+  cuuint32_t box[4] = {inner, 1, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   std::memset(m, 0, sizeof(*m));
   CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   slabs ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -191,8 +195,8 @@ pa_status pa_decode(const pa_config* cfg, const void* q, const void* k_cache, co
 
   const int box_rows = cfg->block_size < v.tt ? cfg->block_size : v.tt;
   CUtensorMap kmap, vmap;
-  if (!kv_tensor_map(&kmap, k_cache, *cfg, box_rows) ||
-      !kv_tensor_map(&vmap, v_cache, *cfg, box_rows))
+  if (!kv_tensor_map(&kmap, k_cache, *cfg, box_rows, v.path == 1) ||
+      !kv_tensor_map(&vmap, v_cache, *cfg, box_rows, v.path == 1))
     return PA_ERR_CUDA;
 
   DecodeArgs a;
@@ -212,7 +216,7 @@ pa_status pa_decode(const pa_config* cfg, const void* q, const void* k_cache, co
   a.q_kind = cfg->q_dtype == PA_FP16 ? Q_FP16 : Q_BF16;
   a.kv_kind = cfg->kv_dtype == PA_FP8_E4M3 ? KV_FP8 : cfg->kv_dtype == PA_FP16 ? KV_FP16 : KV_BF16;
   a.merge_in_decode = cfg->split_merge == PA_MERGE_IN_DECODE;
-  cudaError_t e = launch_decode_simt(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_decode(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

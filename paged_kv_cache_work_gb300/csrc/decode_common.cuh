@@ -1,0 +1,361 @@
+// Pieces shared by the CUDA-core and tensor-core decode kernels: kernel parameters, element
+// conversions, the TMA side of the shared-memory page ring, and the split merge that the last
+// CTA to finish a unit runs inside the decode kernel.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+struct KernelParams {
+  const void* q;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* bt;
+  const int32_t* ctx;
+  const int32_t* qlens;
+  void* out;
+  float* lse;
+  const int32_t* item_off;
+  const int4* items;
+  float* o_part;
+  float* lse_part;
+  int32_t* flags;
+  const int2* unit_info;
+  int32_t* unit_cnt;
+  int units;
+  int merge_in_decode;
+  int scale_mode;
+  int Sq, Hq, Hkv, G, M, RB, bs, maxb, nblocks, causal;
+  int bs_shift;  // log2(bs): pages are a power of two
+  float qk_scale;
+};
+
+// ---- element conversion -----------------------------------------------------------
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ float2 f16x2_to_f2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<__half2*>(&w));
+}
+__device__ __forceinline__ void e4m3x4_to_f2(uint32_t w, float2* f) {
+  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
+  f[0] = __half22float2(*reinterpret_cast<__half2*>(&lo));
+  f[1] = __half22float2(*reinterpret_cast<__half2*>(&hi));
+}
+
+// Raw chunk of cache elements in registers: CB bytes = CB / 4 words.
+template <int CB>
+struct RawChunk {
+  uint32_t w[CB / 4];
+};
+
+template <int CB>
+__device__ __forceinline__ RawChunk<CB> lds_chunk(const char* src) {
+  RawChunk<CB> r;
+  if constexpr (CB == 16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+  } else if constexpr (CB == 8) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    r.w[0] = v.x; r.w[1] = v.y;
+  } else {
+    r.w[0] = *reinterpret_cast<const uint32_t*>(src);
+  }
+  return r;
+}
+
+// Convert a raw chunk of EPC elements to EPC / 2 float2 pairs (element order kept).
+template <int KVK, int CB>
+__device__ __forceinline__ void chunk_to_f2(const RawChunk<CB>& r, float2* f) {
+#pragma unroll
+  for (int j = 0; j < CB / 4; ++j) {
+    if constexpr (KVK == KV_FP8) {
+      e4m3x4_to_f2(r.w[j], f + 2 * j);
+    } else if constexpr (KVK == KV_BF16) {
+      f[j] = bf16x2_to_f2(r.w[j]);
+    } else {
+      f[j] = f16x2_to_f2(r.w[j]);
+    }
+  }
+}
+
+template <int QK>
+__device__ __forceinline__ float2 q_pair(uint32_t w) {
+  if constexpr (QK == Q_BF16)
+    return bf16x2_to_f2(w);
+  else
+    return f16x2_to_f2(w);
+}
+
+template <int QK>
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
+  if constexpr (QK == Q_BF16)
+    reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+}
+
+// The TMA side of the ring, run by warp 0 (all lanes, same state) between its own tiles.
+// R describes the ring: TT tokens per stage of STAGE bytes (K tile of KTILE bytes, then V,
+// then per-token scales when TOKS), NSTAGE stages, and how a tile row is laid out: either
+// one box across the whole head dimension (NSLAB = 1) or NSLAB column slabs of ROWB = 128
+// bytes per row, each written with the 128-byte swizzle.  With WITH_Q the query rows of an
+// item are copied into NQ shared-memory slots together with the item's first tile.
+template <class R>
+struct TileProducer {
+  using T = R;
+  static constexpr int D = R::D;
+  static constexpr int MP = R::MP;
+  static constexpr bool TOKS = R::TOKS;
+  const KernelParams* p;
+  const CUtensorMap* kmap;
+  const CUtensorMap* vmap;
+  char* smem;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* qfull;
+  volatile int* abort_flag;
+  int lane, it, it_end;
+  int k, ntiles, t0, t1, b, g, rb;
+  uint32_t issued, items_started;
+  int box_rows, nbox;  // rows per box (one page or one tile), boxes (pages) per tile
+  uint32_t box_bytes;  // bytes of one box
+  int blk_next;
+  bool have;        // current item has tiles left
+  bool next_ready;  // blk_next already holds the next item's first-tile block ids
+  int4 item_next;
+
+  // lane -> (page of the tile, column slab): lane = page * NSLAB + slab
+  __device__ __forceinline__ int box_block_of(int bb, int tt0, int tt1, int kk) const {
+    const int tokb = tt0 + kk * T::TT + (lane / T::NSLAB) * box_rows;
+    return (lane < nbox * T::NSLAB && tokb < tt1)
+               ? __ldg(p->bt + (size_t)bb * p->maxb + (tokb >> p->bs_shift))
+               : -1;
+  }
+  __device__ __forceinline__ int box_block(int kk) const { return box_block_of(b, t0, t1, kk); }
+
+  __device__ __forceinline__ void init(const KernelParams* prm, const CUtensorMap* km,
+                                       const CUtensorMap* vm, char* sm, uint64_t* f,
+                                       uint64_t* e, uint64_t* qf, volatile int* ab, int ln,
+                                       int ib, int ie) {
+    p = prm; kmap = km; vmap = vm; smem = sm; full = f; empty = e; qfull = qf; abort_flag = ab;
+    lane = ln; it = ib - 1; it_end = ie; k = 0; ntiles = 0; issued = 0; items_started = 0;
+    box_rows = min(p->bs, T::TT);
+    nbox = T::TT / box_rows;
+    box_bytes = (uint32_t)box_rows * T::ROWB;
+    have = false;
+    next_ready = false;
+    item_next = ib < ie ? p->items[ib] : make_int4(0, 0, 0, -1);
+  }
+
+  // Move to the next item with tokens; false when the CTA's list is exhausted.
+  __device__ __forceinline__ bool advance() {
+    while (!have) {
+      if (++it >= it_end) return false;
+      const int4 item = item_next;
+      if (it + 1 < it_end) item_next = p->items[it + 1];
+      t0 = item.y;
+      t1 = item.z;
+      if (t1 <= t0) continue;
+      const int u = item.x;
+      b = u / (p->Hkv * p->RB);
+      g = (u / p->RB) % p->Hkv;
+      rb = u % p->RB;
+      k = 0;
+      ntiles = ceil_div(t1 - t0, T::TT);
+      if (!next_ready) blk_next = box_block(0);
+      next_ready = false;
+      have = true;
+    }
+    return true;
+  }
+
+  // Issue the next tile of the CTA's sequence into its stage (waiting for the stage to be
+  // released by every warp); the query rows of an item go out with its first tile.
+  __device__ __forceinline__ bool issue_one() {
+    if (!advance()) return false;
+    const int s = issued % T::NSTAGE;
+    const uint32_t ph = (issued / T::NSTAGE) & 1;
+    const int tok0 = t0 + k * T::TT;
+    const int page = lane / T::NSLAB, slab = lane % T::NSLAB;
+    const int tokb = tok0 + page * box_rows;
+    const int blk = blk_next;
+    const bool want = lane < nbox * T::NSLAB && tokb < t1;
+    const bool ok = want && blk >= 0 && blk < p->nblocks;
+    if (want && !ok) atomicOr(p->flags, PA_FLAG_BAD_BLOCK_ID);
+    const uint32_t nvalid = __popc(__ballot_sync(kFull, ok));
+    // overlap the next lookup: the next tile of this item, or the first of the next item
+    if (k + 1 < ntiles) {
+      blk_next = box_block(k + 1);
+    } else if (it + 1 < it_end && item_next.z > item_next.y) {
+      blk_next = box_block_of(item_next.x / (p->Hkv * p->RB), item_next.y, item_next.z, 0);
+      next_ready = true;
+    }
+    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+      atomicOr(p->flags, PA_FLAG_WAIT_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+    if (T::WITH_Q && k == 0) {
+      // query rows of this item: MP rows x D, 16-byte cp.async, completing on qfull
+      const int qs = items_started % T::NQ;
+      ++items_started;
+      char* qslot = smem + T::OFF_Q + qs * T::QSLOT;
+      constexpr int QCH = D * 2 / 16;
+      for (int c = lane; c < MP * QCH; c += 32) {
+        const int r = c / QCH, cc = c % QCH, rg = rb * MP + r;
+        if (rg < p->M) {
+          const int i = rg / p->G, gq = rg % p->G;
+          const char* src = reinterpret_cast<const char*>(p->q) +
+                            ((((size_t)b * p->Sq + i) * p->Hq + (size_t)g * p->G + gq) * D) * 2 +
+                            cc * 16;
+          cp_async_16(qslot + r * D * 2 + cc * 16, src);
+        }
+      }
+      cp_async_arrive_noinc(&qfull[qs]);
+    }
+    char* st = smem + s * T::STAGE;
+    if (lane == 0) mbar_arrive_expect_tx(&full[s], nvalid * 2u * box_bytes);
+    __syncwarp();
+    if (ok) {
+      // slab h of page j lands at h * (TT rows) + j * (box rows), in units of ROWB bytes
+      const int row = tokb & (p->bs - 1);
+      const uint32_t dst = (uint32_t)(slab * T::TT + page * box_rows) * T::ROWB;
+      const int x = slab * (T::ROWB / T::BPE);
+      tma_load_4d(st + dst, kmap, &full[s], x, g, row, blk);
+      tma_load_4d(st + T::KTILE + dst, vmap, &full[s], x, g, row, blk);
+    }
+    if constexpr (TOKS) {
+      float* sks = reinterpret_cast<float*>(st + 2 * T::KTILE);
+      float* svs = sks + T::TT;
+      for (int t = lane; t < T::TT; t += 32) {
+        const int bb = __shfl_sync(kFull, blk, (t / box_rows) * T::NSLAB);
+        const int tok = tok0 + t;
+        if (tok < t1 && bb >= 0 && bb < p->nblocks) {
+          const size_t idx = ((size_t)bb * p->bs + (tok & (p->bs - 1))) * p->Hkv + g;
+          cp_async_4(sks + t, p->k_scale + idx);
+          cp_async_4(svs + t, p->v_scale + idx);
+        }
+      }
+      cp_async_arrive_noinc(&full[s]);
+    }
+    ++issued;
+    if (++k >= ntiles) have = false;
+    return true;
+  }
+
+  // Keep the ring filled up to tile `upto` (global tile index of this CTA).
+  __device__ __forceinline__ void fill(uint32_t upto) {
+    while (issued <= upto && !*abort_flag) {
+      if (!issue_one()) break;
+    }
+  }
+
+  // Let every copy this warp started land before the CTA may exit.
+  __device__ __forceinline__ void drain() {
+    cp_async_wait_all();
+    const uint32_t first = issued > (uint32_t)T::NSTAGE ? issued - T::NSTAGE : 0;
+    for (uint32_t j = first; j < issued; ++j)
+      mbar_wait_drain(&full[j % T::NSTAGE], (j / T::NSTAGE) & 1);
+  }
+};
+
+// The split merge inside the decode kernel: after a CTA has written its partial of unit u,
+// it counts itself in; the CTA that brings the count to the number of pieces merges every
+// piece of the unit (its own last) with the log-sum-exp rule and writes the output.  No CTA
+// waits for another: the ones that are not last simply move on.  The fences order each
+// CTA's partial writes before its arrival and the merging CTA's reads after it; partials are
+// read through L2 (ld.global.cg), where other SMs' writes are visible.
+template <int D, int MP, int QK, int NW>
+__device__ __forceinline__ void merge_if_last(const KernelParams& p, int u, int b, int g, int rb,
+                                              float* wtab, int wcap, float* stat,
+                                              volatile int* last_flag) {
+  constexpr int NT = NW * 32;
+  const int2 info = __ldg(&p.unit_info[u]);
+  const int first = info.x, ns = info.y;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int before = atomicAdd(&p.unit_cnt[u], 1);
+    *last_flag = before == ns - 1;
+  }
+  named_barrier_sync(1, NT);
+  if (!*last_flag) return;
+  __threadfence();
+  const bool tab = MP * ns <= wcap;  // weights fit in shared memory
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // per row: max and weight sum over the pieces (lanes over pieces)
+  for (int r = warp; r < MP; r += NW) {
+    float m = -INFINITY;
+    for (int s = lane; s < ns; s += 32)
+      m = fmaxf(m, __ldcg(p.lse_part + (size_t)piece_slot(first, s) * MP + r));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    float W = 0.f;
+    for (int s = lane; s < ns; s += 32) {
+      const float ls = __ldcg(p.lse_part + (size_t)piece_slot(first, s) * MP + r);
+      const float w = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+      if (tab) wtab[r * ns + s] = w;
+      W += w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
+    if (lane == 0) {
+      stat[2 * r] = m;
+      stat[2 * r + 1] = W;
+    }
+  }
+  named_barrier_sync(1, NT);
+  for (int e = threadIdx.x; e < MP * D; e += NT) {
+    const int r = e / D, d = e % D, rg = rb * MP + r;
+    if (rg >= p.M) continue;
+    const float m = stat[2 * r], W = stat[2 * r + 1];
+    float O = 0.f;
+    if (W > 0.f) {
+#pragma unroll 4
+      for (int s = 0; s < ns; ++s) {
+        const size_t part = (size_t)piece_slot(first, s) * MP + r;
+        float w;
+        if (tab) {
+          w = wtab[r * ns + s];
+        } else {
+          const float ls = __ldcg(p.lse_part + part);
+          w = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+        }
+        O += w * __ldcg(p.o_part + part * D + d);
+      }
+    }
+    const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
+    store_out<QK>(p.out, row * D + d, W > 0.f ? O / W : 0.f);
+    if (d == 0 && p.lse) p.lse[row] = W > 0.f ? (m + fast_log2(W)) * kLn2 : -INFINITY;
+  }
+  named_barrier_sync(1, NT);  // the shared buffers are reused by the next item
+}
+
+// Units with no keys at all: padding rows (zero, lse = -inf), spread over the CTAs.
+template <int D, int MP, int QK, int NT>
+__device__ __forceinline__ void zero_empty_units(const KernelParams& p) {
+  for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+    if (__ldg(&p.unit_info[u].y) != 0) continue;
+    const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
+    for (int e = threadIdx.x; e < MP * D; e += NT) {
+      const int r = e / D, d = e % D, rg = rb * MP + r;
+      if (rg >= p.M) continue;
+      const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
+      store_out<QK>(p.out, row * D + d, 0.f);
+      if (d == 0 && p.lse) p.lse[row] = -INFINITY;
+    }
+  }
+}
+
+KernelParams make_kernel_params(const DecodeArgs& a);
+
+}  // namespace pa

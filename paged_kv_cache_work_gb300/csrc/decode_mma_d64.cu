@@ -1,0 +1,16 @@
+// Tensor-core decode kernel instances for head dim 64 (one translation unit per head dim
+// so the instances compile in parallel).
+#include "decode_mma.cuh"
+
+namespace pa {
+
+cudaError_t launch_mma_d64(const KernelParams& prm, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          int grid, int mp, int kvk, int qk, bool toks, cudaStream_t s) {
+  return launch_mma_for_dim<64>(prm, kmap, vmap, grid, mp, kvk, qk, toks, s);
+}
+
+int mma_ctas_per_sm_d64(int mp, int kvk, bool toks) {
+  return mma_ctas_per_sm_for_dim<64>(mp, kvk, toks);
+}
+
+}  // namespace pa

@@ -4,7 +4,7 @@
 
 namespace pa {
 
-cudaError_t launch_simt_d256(const SimtParams& prm, const CUtensorMap& kmap, const CUtensorMap& vmap,
+cudaError_t launch_simt_d256(const KernelParams& prm, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int grid, int mp, int kvk, int qk, bool toks, cudaStream_t s) {
   return launch_simt_for_dim<256>(prm, kmap, vmap, grid, mp, kvk, qk, toks, s);
 }

@@ -27,6 +27,7 @@ __host__ __device__ constexpr size_t round_up_sz(size_t a, size_t b) { return (a
 // tiles of `mp` (a power of two); a unit of work is one (sequence, kv head, row
 // tile), and `tt` is the number of tokens staged per pipeline stage.
 struct Variant {
+  int path;         // 0: CUDA-core kernel (rows <= 8), 1: tensor-core kernel
   int rows;         // M = G * Sq
   int mp;           // rows per unit (padded to a power of two)
   int rb;           // row tiles per kv head
@@ -48,20 +49,32 @@ inline int pow2_at_least(int x) {
   return p;
 }
 
-// CTAs of the CUDA-core decode instance for these parameters that fit on one SM.
+// CTAs of the decode instance for these parameters that fit on one SM.
 int simt_ctas_per_sm(int head_dim, int mp, int kvk, bool toks);
+int mma_ctas_per_sm(int head_dim, int mp, int kvk, bool toks);
+// Largest row tile of the tensor-core decode kernel.
+constexpr int kMmaMaxRows = 64;
 
 // Everything but the grid size, which needs the device (see api.cu).
+// Query tiles of more than 8 rows per kv head run on tensor cores (padded to 16, 32 or 64
+// rows; larger groups are cut into 64-row tiles); the tensor-core kernel needs a tile row of
+// at least one 128-byte slab, so a 64-dim fp8 cache stays on the CUDA-core kernel.
 inline Variant make_variant(const pa_config& c) {
   Variant v{};
   v.rows = (c.num_q_heads / c.num_kv_heads) * c.max_q_len;
-  v.mp = v.rows <= kSimtMaxRows ? pow2_at_least(v.rows) : kSimtMaxRows;
-  v.rb = ceil_div(v.rows, v.mp);
   v.bpe = c.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
+  v.path = (v.rows > kSimtMaxRows && c.head_dim * v.bpe >= 128) ? 1 : 0;
+  if (v.path == 1)
+    v.mp = v.rows >= kMmaMaxRows ? kMmaMaxRows : (v.rows <= 16 ? 16 : pow2_at_least(v.rows));
+  else
+    v.mp = v.rows <= kSimtMaxRows ? pow2_at_least(v.rows) : kSimtMaxRows;
+  v.rb = ceil_div(v.rows, v.mp);
   v.tt = kTileBytes / (c.head_dim * v.bpe);
   v.units = c.batch * c.num_kv_heads * v.rb;
   const int kvk = c.kv_dtype == PA_FP8_E4M3 ? 2 : (c.kv_dtype == PA_FP16 ? 1 : 0);
-  v.ctas_per_sm = simt_ctas_per_sm(c.head_dim, v.mp, kvk, c.kv_scale_mode == PA_SCALE_PER_TOKEN);
+  const bool toks = c.kv_scale_mode == PA_SCALE_PER_TOKEN;
+  v.ctas_per_sm = v.path == 1 ? mma_ctas_per_sm(c.head_dim, v.mp, kvk, toks)
+                              : simt_ctas_per_sm(c.head_dim, v.mp, kvk, toks);
   v.ctas = 0;
   return v;
 }
@@ -169,8 +182,8 @@ struct DecodeArgs {
 };
 
 // Returns cudaErrorNotSupported when no kernel instance matches.
-cudaError_t launch_decode_simt(const DecodeArgs& a, const CUtensorMap& kmap,
-                               const CUtensorMap& vmap, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t s);
 
 cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s);
 

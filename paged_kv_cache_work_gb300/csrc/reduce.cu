@@ -11,15 +11,25 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "decode_simt.cuh"
+#include "decode_common.cuh"
 
 namespace pa {
 
-cudaError_t launch_simt_d64(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+cudaError_t launch_simt_d64(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                             int, int, bool, cudaStream_t);
 int simt_ctas_per_sm_d64(int, int, bool);
 int simt_ctas_per_sm_d128(int, int, bool);
 int simt_ctas_per_sm_d256(int, int, bool);
+
+int mma_ctas_per_sm_d64(int, int, bool);
+int mma_ctas_per_sm_d128(int, int, bool);
+int mma_ctas_per_sm_d256(int, int, bool);
+cudaError_t launch_mma_d64(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+                           int, int, bool, cudaStream_t);
+cudaError_t launch_mma_d128(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+                            int, int, bool, cudaStream_t);
+cudaError_t launch_mma_d256(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+                            int, int, bool, cudaStream_t);
 
 int simt_ctas_per_sm(int head_dim, int mp, int kvk, bool toks) {
   switch (head_dim) {
@@ -28,13 +38,21 @@ int simt_ctas_per_sm(int head_dim, int mp, int kvk, bool toks) {
     default: return simt_ctas_per_sm_d256(mp, kvk, toks);
   }
 }
-cudaError_t launch_simt_d128(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+
+int mma_ctas_per_sm(int head_dim, int mp, int kvk, bool toks) {
+  switch (head_dim) {
+    case 64: return mma_ctas_per_sm_d64(mp, kvk, toks);
+    case 128: return mma_ctas_per_sm_d128(mp, kvk, toks);
+    default: return mma_ctas_per_sm_d256(mp, kvk, toks);
+  }
+}
+cudaError_t launch_simt_d128(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                              int, int, bool, cudaStream_t);
-cudaError_t launch_simt_d256(const SimtParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+cudaError_t launch_simt_d256(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                              int, int, bool, cudaStream_t);
 
-SimtParams make_simt_params(const DecodeArgs& a) {
-  SimtParams p{};
+KernelParams make_kernel_params(const DecodeArgs& a) {
+  KernelParams p{};
   p.q = a.q;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
@@ -68,10 +86,18 @@ SimtParams make_simt_params(const DecodeArgs& a) {
   return p;
 }
 
-cudaError_t launch_decode_simt(const DecodeArgs& a, const CUtensorMap& kmap,
-                               const CUtensorMap& vmap, cudaStream_t s) {
-  const SimtParams prm = make_simt_params(a);
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t s) {
+  const KernelParams prm = make_kernel_params(a);
   const bool toks = a.scale_mode == PA_SCALE_PER_TOKEN;
+  if (a.v.path == 1) {
+    switch (a.p.head_dim) {
+      case 64: return launch_mma_d64(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+      case 128: return launch_mma_d128(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+      case 256: return launch_mma_d256(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+      default: return cudaErrorNotSupported;
+    }
+  }
   switch (a.p.head_dim) {
     case 64: return launch_simt_d64(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
     case 128: return launch_simt_d128(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);

@@ -70,9 +70,12 @@ TILE_BYTES = 16384
 
 def variant(cfg: pa.PaConfig, ctas: int):
     rows = (cfg.num_q_heads // cfg.num_kv_heads) * cfg.max_q_len
-    mp = _pow2_at_least(rows) if rows <= SIMT_MAX_ROWS else SIMT_MAX_ROWS
-    rb = -(-rows // mp)
     bpe = 1 if cfg.kv_dtype == pa.FP8_E4M3 else 2
+    if rows > SIMT_MAX_ROWS and cfg.head_dim * bpe >= 128:  # tensor-core kernel
+        mp = 64 if rows >= 64 else (16 if rows <= 16 else _pow2_at_least(rows))
+    else:
+        mp = _pow2_at_least(rows) if rows <= SIMT_MAX_ROWS else SIMT_MAX_ROWS
+    rb = -(-rows // mp)
     tt = TILE_BYTES // (cfg.head_dim * bpe)
     return dict(rows=rows, mp=mp, rb=rb, tt=tt, units=cfg.batch * cfg.num_kv_heads * rb,
                 ctas=ctas)

@@ -123,6 +123,28 @@ EDGE = [
                             block_size=16, ctx=[257, 900])),
     ("rows_3_padded", dict(batch=2, max_q_len=3, num_q_heads=2, num_kv_heads=2, head_dim=256,
                            block_size=32, ctx=[100, 64], causal=True)),
+    # tensor-core kernel (more than 8 query rows per kv head)
+    ("mma_rows12_padded", dict(batch=3, max_q_len=1, num_q_heads=24, num_kv_heads=2,
+                               head_dim=128, block_size=16, ctx=[77, 300, 16])),
+    ("mma_rows100_two_tiles", dict(batch=2, max_q_len=4, num_q_heads=25, num_kv_heads=1,
+                                   head_dim=128, block_size=64, ctx=[200, 517], causal=True)),
+    ("mma_fp16_rows32", dict(batch=2, max_q_len=2, num_q_heads=16, num_kv_heads=1, head_dim=128,
+                             block_size=32, ctx=[150, 333], q_dtype="fp16", kv_dtype="fp16",
+                             causal=True)),
+    ("mma_d64_rows32", dict(batch=2, max_q_len=4, num_q_heads=8, num_kv_heads=1, head_dim=64,
+                            block_size=128, ctx=[130, 700], causal=True)),
+    ("mma_fp8_d256_rows16", dict(batch=2, max_q_len=16, num_q_heads=2, num_kv_heads=2,
+                                 head_dim=256, block_size=32, ctx=[40, 300], kv_dtype="fp8",
+                                 scale_mode="token", causal=True)),
+    ("mma_fp8_tensor_rows64", dict(batch=2, max_q_len=4, num_q_heads=16, num_kv_heads=1,
+                                   head_dim=128, block_size=256, ctx=[260, 1000],
+                                   kv_dtype="fp8", scale_mode="tensor", causal=True)),
+    ("mma_fp8_fp16q_rows32", dict(batch=2, max_q_len=2, num_q_heads=16, num_kv_heads=1,
+                                  head_dim=128, block_size=16, ctx=[99, 180], q_dtype="fp16",
+                                  kv_dtype="fp8", scale_mode="none")),
+    ("mma_d64_fp8_stays_on_cuda_cores", dict(batch=2, max_q_len=1, num_q_heads=16,
+                                             num_kv_heads=1, head_dim=64, block_size=16,
+                                             ctx=[70, 130], kv_dtype="fp8", scale_mode="token")),
 ]
 
 

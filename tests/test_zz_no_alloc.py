@@ -19,8 +19,9 @@ from gpu_run import compare
 
 pytestmark = pytest.mark.gpu
 
-CASES = [W.reduced(W.GQA_B32, 6, 300, 2500), W.reduced(W.LONG_SQ4, 2, 3000, 9000),
-         W.reduced(W.FP8_TOKEN_SQ1, 4, 1000, 4000), W.reduced(W.mha_d256(8, 4), 3, 200, 1500)]
+CASES = [W.reduced(W.GQA_B32, 6, 300, 2500), W.reduced(W.LONG_SQ1, 2, 3000, 9000),
+         W.reduced(W.FP8_TOKEN_SQ1, 4, 1000, 4000), W.reduced(W.mha_d256(8, 4), 3, 200, 1500),
+         W.reduced(W.mha_d256(8, 16), 2, 200, 900)]
 
 
 def _static_call(lib, cfg, inp, out, lse):
