@@ -43,9 +43,29 @@ if ROOT not in sys.path:
 
 METRIC = "decode µs/call and achieved HBM TB/s on KV bytes read vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_KERNEL = "decode_simt_kernel"
 KERNEL_SOURCES = ["paged_kv_cache_work_gb300/csrc/decode_simt.cuh",
+                  "paged_kv_cache_work_gb300/csrc/decode_mma.cuh",
+                  "paged_kv_cache_work_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_work_gb300/csrc/pa_internal.cuh"]
+
+
+def decode_shape(wl):
+    """(decode kernel name, rows per unit) the library picks for a workload: caches with a
+    tile row of at least 128 bytes go to the tensor-core kernel in query tiles of 16, 32 or
+    64 rows, the rest (64-dim fp8) to the CUDA-core kernel in tiles of up to 8 rows."""
+    rows = (wl.num_q_heads // wl.num_kv_heads) * wl.max_q_len
+    bpe = 1 if wl.kv_dtype == "fp8" else 2
+    pow2 = 1 << max(0, (rows - 1).bit_length())
+    if wl.head_dim * bpe >= 128:
+        return "decode_mma_kernel", 64 if rows >= 64 else max(16, pow2)
+    return "decode_simt_kernel", min(pow2, 8)
+
+
+def launches_per_step(split_merge: int) -> int:
+    """Kernels one plan/decode/reduce step launches: pa_reduce launches its kernel unless
+    every split unit is merged inside the decode (PA_MERGE_IN_DECODE)."""
+    import paged_kv_cache_work_gb300 as pa
+    return 2 if split_merge == pa.MERGE_IN_DECODE else 3
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -372,10 +392,11 @@ def run_ours(args, rank, world, local):
                 "l2": (f"inputs larger than L2: 2 input sets of {int(bytes_per_launch) >> 20} MiB KV "
                        f"alternate (L2 {l2 >> 20} MiB)"),
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                "split_merge": "in decode (last CTA of a unit merges)",
+                "split_merge": "auto (decode's last CTA merges units of few pieces, "
+                               "the reduce kernel the rest)",
             },
             "roofline": {
-                "kernel": DECODE_KERNEL, "bound": "hbm", "achieved": round(achieved_gbs, 1),
+                "kernel": decode_shape(wl)[0], "bound": "hbm", "achieved": round(achieved_gbs, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
@@ -386,7 +407,7 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": round(e2e_all / e2e_s / 1e12, 4), "unit": "TB/s",
                     "us_per_call": round(e2e_s / n_e2e * 1e6, 2), "steps": n_e2e,
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": launches_per_step(cfg.split_merge) * args.steps,
             "timing": "device time of K CUDA-graph replays of the step (plan, decode, reduce)",
             "clocks": clocks,
         }

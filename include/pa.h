@@ -79,12 +79,17 @@ typedef enum {
   PA_SCALE_PER_TOKEN = 2   /* k_scale, v_scale: fp32 [num_blocks, block_size, num_kv_heads] */
 } pa_scale_mode;
 
-/* Where the log-sum-exp merge of split units runs.  PA_MERGE_IN_DECODE (the default, 0):
- * the last CTA to finish a piece of a unit merges that unit's partials inside pa_decode
- * (an atomic arrival counter per unit; no CTA ever waits for another), so pa_decode leaves
- * the finished output and pa_reduce launches nothing.  PA_MERGE_IN_REDUCE: pa_decode only
- * writes the partials and pa_reduce merges them in its own kernel. */
-typedef enum { PA_MERGE_IN_DECODE = 0, PA_MERGE_IN_REDUCE = 1 } pa_split_merge;
+/* Where the log-sum-exp merge of split units runs.  A unit cut into ns pieces can be merged
+ * by the last CTA to finish one of its pieces, inside pa_decode (an atomic arrival counter
+ * per unit; no CTA ever waits for another), or by pa_reduce's own kernel, which spreads the
+ * rows of the unit over many CTAs.  The first costs no launch but runs on one SM, so it
+ * suits units of a few pieces; the second suits units cut into many.
+ *   PA_MERGE_AUTO (0, the default): pa_decode merges a unit when its partials are small
+ *     (ns * row tile * head_dim <= 32768 floats, or ns <= 2); pa_reduce merges the rest.
+ *   PA_MERGE_IN_DECODE: pa_decode merges every unit and pa_reduce launches nothing.
+ *   PA_MERGE_IN_REDUCE: pa_decode only writes partials and pa_reduce merges them all.
+ * The choice changes the order of no sum inside a merge: outputs agree to rounding. */
+typedef enum { PA_MERGE_AUTO = 0, PA_MERGE_IN_DECODE = 1, PA_MERGE_IN_REDUCE = 2 } pa_split_merge;
 
 /* Device-side input problems, OR-ed into the flags word. */
 enum {
@@ -134,18 +139,19 @@ PA_API pa_status pa_plan(const pa_config *cfg, const int32_t *block_tables, cons
  *   k_cache  [num_blocks, block_size, Hkv, D]   kv_dtype (uint8 codes for fp8)
  *   v_cache  same layout as k_cache
  *   k_scale, v_scale  NULL unless fp8 with a scale mode (see pa_scale_mode)
- *   out      [B, Sq, Hq, D]            q_dtype; written for units done in one piece
+ *   out      [B, Sq, Hq, D]            q_dtype; written for every unit done in one piece,
+ *            with no keys, or merged here (see pa_split_merge)
  *   lse      [B, Sq, Hq] fp32 natural-log LSE, or NULL
- * The tables and lengths must be the ones given to pa_plan. */
+ * The tables and lengths must be the ones given to pa_plan.  A decode that completed leaves
+ * the merge counters as pa_plan set them, so pa_decode may run again on the same plan. */
 PA_API pa_status pa_decode(const pa_config *cfg, const void *q, const void *k_cache, const void *v_cache,
                     const float *k_scale, const float *v_scale, const int32_t *block_tables,
                     const int32_t *context_lens, const int32_t *q_lens, void *out, float *lse,
                     void *ws, size_t ws_bytes, pa_stream stream);
 
-/* Completes the step.  With PA_MERGE_IN_REDUCE: merges the split partials of every unit
- * pa_decode left in ws into out (and lse) and writes the padding rows of units with no keys.
- * With PA_MERGE_IN_DECODE pa_decode has already done both, and this call only validates its
- * arguments and launches nothing. */
+/* Completes the step: merges the split partials pa_decode left in ws into out (and lse) for
+ * every unit pa_decode did not merge itself (see pa_split_merge).  With PA_MERGE_IN_DECODE
+ * there is none, and this call only validates its arguments and launches nothing. */
 PA_API pa_status pa_reduce(const pa_config *cfg, void *out, float *lse, void *ws, size_t ws_bytes,
                     pa_stream stream);
 

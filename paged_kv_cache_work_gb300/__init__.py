@@ -19,7 +19,7 @@ __all__ = ["PaConfig", "PaError", "load", "workspace_size", "plan", "decode", "r
            "read_flags", "status_string", "config_for", "paged_attention", "LIB_PATH",
            "BF16", "FP16", "FP8_E4M3", "SCALE_NONE", "SCALE_PER_TENSOR", "SCALE_PER_TOKEN",
            "FLAG_BAD_LENGTHS", "FLAG_BAD_BLOCK_ID", "FLAG_WAIT_TIMEOUT", "EXPORTED_SYMBOLS",
-           "MERGE_IN_DECODE", "MERGE_IN_REDUCE"]
+           "MERGE_AUTO", "MERGE_IN_DECODE", "MERGE_IN_REDUCE"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpa103.so")
@@ -30,7 +30,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = rang
 BF16, FP16, FP8_E4M3 = 0, 1, 2
 SCALE_NONE, SCALE_PER_TENSOR, SCALE_PER_TOKEN = 0, 1, 2
 FLAG_BAD_LENGTHS, FLAG_BAD_BLOCK_ID, FLAG_WAIT_TIMEOUT = 1, 2, 4
-MERGE_IN_DECODE, MERGE_IN_REDUCE = 0, 1
+MERGE_AUTO, MERGE_IN_DECODE, MERGE_IN_REDUCE = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("pa_workspace_size", "pa_plan", "pa_decode", "pa_reduce", "pa_read_flags",
                     "pa_status_string", "pa_decode_step_static")
@@ -160,7 +160,7 @@ _SM = {"none": SCALE_NONE, "tensor": SCALE_PER_TENSOR, "token": SCALE_PER_TOKEN}
 
 
 def config_for(inp: dict, num_ctas: int = 0, grid_mult: int = 0,
-               split_merge: int = MERGE_IN_DECODE) -> PaConfig:
+               split_merge: int = MERGE_AUTO) -> PaConfig:
     """pa_config of a problem laid out as workloads.make_inputs returns it."""
     w = inp["workload"]
     return PaConfig(batch=w.batch, max_q_len=w.max_q_len, num_q_heads=w.num_q_heads,

@@ -34,7 +34,7 @@ pa_status validate(const pa_config* c) {
   if (c->causal != 0 && c->causal != 1) return PA_ERR_INVALID_ARG;
   if (!std::isfinite(c->sm_scale)) return PA_ERR_INVALID_ARG;
   if (c->num_ctas < 0 || c->grid_mult < 0) return PA_ERR_INVALID_ARG;
-  if (c->split_merge != PA_MERGE_IN_DECODE && c->split_merge != PA_MERGE_IN_REDUCE)
+  if (c->split_merge < PA_MERGE_AUTO || c->split_merge > PA_MERGE_IN_REDUCE)
     return PA_ERR_INVALID_ARG;
   if (c->num_q_heads % c->num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return PA_ERR_UNSUPPORTED;
@@ -50,18 +50,19 @@ pa_status validate(const pa_config* c) {
 
 // Persistent grid: num_ctas if given, else (SMs x grid_mult) x the decode CTAs that fit
 // on one SM, so the whole grid is resident at once.
-pa_status resolve_ctas(const pa_config& c, const Variant& v, int* ctas) {
+pa_status resolve_ctas(const pa_config& c, Variant* v) {
   if (c.num_ctas > 0) {
-    *ctas = c.num_ctas > 65535 ? 65535 : c.num_ctas;
+    v->ctas = c.num_ctas > 65535 ? 65535 : c.num_ctas;
     return PA_OK;
   }
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PA_ERR_CUDA;
+  v->sms = sms;
   const int mult = c.grid_mult > 0 ? c.grid_mult : 1;
-  long long n = (long long)sms * mult * v.ctas_per_sm;
-  *ctas = (int)(n > 65535 ? 65535 : n);
+  long long n = (long long)sms * mult * v->ctas_per_sm;
+  v->ctas = (int)(n > 65535 ? 65535 : n);
   return PA_OK;
 }
 
@@ -69,10 +70,11 @@ pa_status prepare(const pa_config* cfg, Variant* v, WsLayout* L) {
   pa_status st = validate(cfg);
   if (st != PA_OK) return st;
   *v = make_variant(*cfg);
-  st = resolve_ctas(*cfg, *v, &v->ctas);
+  st = resolve_ctas(*cfg, v);
   if (st != PA_OK) return st;
   // The planner's concatenated token space is indexed with int32.
-  const long long per_unit = (long long)round_up(cfg->max_blocks_per_seq, 1) * cfg->block_size + v->tt;
+  const long long per_unit =
+      (long long)cfg->max_blocks_per_seq * cfg->block_size + v->tt + v->item_cost;
   if ((long long)v->units * per_unit >= (1ll << 30)) return PA_ERR_UNSUPPORTED;
   *L = ws_layout(*cfg, *v);
   return PA_OK;
@@ -215,7 +217,6 @@ pa_status pa_decode(const pa_config* cfg, const void* q, const void* k_cache, co
   a.v = v;
   a.q_kind = cfg->q_dtype == PA_FP16 ? Q_FP16 : Q_BF16;
   a.kv_kind = cfg->kv_dtype == PA_FP8_E4M3 ? KV_FP8 : cfg->kv_dtype == PA_FP16 ? KV_FP16 : KV_BF16;
-  a.merge_in_decode = cfg->split_merge == PA_MERGE_IN_DECODE;
   cudaError_t e = launch_decode(a, kmap, vmap, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

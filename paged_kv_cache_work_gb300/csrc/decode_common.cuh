@@ -31,7 +31,7 @@ struct KernelParams {
   const int2* unit_info;
   int32_t* unit_cnt;
   int units;
-  int merge_in_decode;
+  int ns_dec;  // split units of at most this many pieces are merged here (see merge_if_last)
   int scale_mode;
   int Sq, Hq, Hkv, G, M, RB, bs, maxb, nblocks, causal;
   int bs_shift;  // log2(bs): pages are a power of two
@@ -102,6 +102,22 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v) {
     reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
   else
     reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+}
+
+// Four consecutive outputs (idx a multiple of 4: one 8-byte store).
+template <int QK>
+__device__ __forceinline__ void store_out4(void* out, size_t idx, float4 v) {
+  uint2 w;
+  if constexpr (QK == Q_BF16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    w.x = *reinterpret_cast<uint32_t*>(&a);
+    w.y = *reinterpret_cast<uint32_t*>(&b);
+  } else {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    w.x = *reinterpret_cast<uint32_t*>(&a);
+    w.y = *reinterpret_cast<uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint2*>(static_cast<char*>(out) + idx * 2) = w;
 }
 
 // The TMA side of the ring, run by warp 0 (all lanes, same state) between its own tiles.
@@ -269,56 +285,89 @@ struct TileProducer {
   }
 };
 
-// The split merge inside the decode kernel: after a CTA has written its partial of unit u,
-// it counts itself in; the CTA that brings the count to the number of pieces merges every
-// piece of the unit (its own last) with the log-sum-exp rule and writes the output.  No CTA
-// waits for another: the ones that are not last simply move on.  The fences order each
-// CTA's partial writes before its arrival and the merging CTA's reads after it; partials are
-// read through L2 (ld.global.cg), where other SMs' writes are visible.
+// ---- split units ----------------------------------------------------------------------
+// A unit cut into ns pieces is merged inside the decode kernel when ns <= ns_dec (larger
+// ones are left to the reduce kernel).  unit_cnt[u] counts the pieces whose partial
+// (o_part, lse_part) is published.  When piece 0 ends and finds every other piece published
+// (count == ns - 1, read with acquire), it is the last: it combines the others' partials with
+// its own state in registers and writes the output, without publishing.  Any other piece
+// writes its partial and publishes it with an acquire-release add; the add that returns
+// ns - 1 belongs to a piece that turned out last after all, and that CTA merges the unit from
+// the partials after its own work list (the add's result is only waited for there).
+// Exactly one piece merges each unit, no CTA ever waits for another, and the merging CTA
+// sets the count back to zero, so the next decode on the same plan starts clean.
+//
+// Both ways of merging do the same arithmetic, so the result does not depend on which piece
+// ends last: per row m = max_s l_s, w_s = 2^(l_s - m) (0 for l_s = -inf), W = sum of w_s
+// added in piece order, O = fma(w_s, o_s, O) in piece order from O = 0, out = O * (1 / W),
+// where o_s is a piece's normalised partial exactly as it is stored.
+constexpr int kFlagBytes = 32;  // abort flag, pending merges, count seen (after the barriers)
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* ptr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v)
+               : "memory");
+  return old;
+}
+// Piece index of `slot` within a unit whose first piece sits in slot `first`.
+__device__ __forceinline__ int piece_index(int first, int slot) {
+  return slot == first ? 0 : (slot >> 1) - (first >> 1);
+}
+
+// Merge every published piece of unit u with the log-sum-exp rule and write its output
+// rows, then reset its count.  All NW warps of the CTA take part.
 template <int D, int MP, int QK, int NW>
-__device__ __forceinline__ void merge_if_last(const KernelParams& p, int u, int b, int g, int rb,
-                                              float* wtab, int wcap, float* stat,
-                                              volatile int* last_flag) {
+__device__ __forceinline__ void merge_unit(const KernelParams& p, int u, float* wtab, int wcap,
+                                           float* stat) {
   constexpr int NT = NW * 32;
+  constexpr int D4 = D / 4;
   const int2 info = __ldg(&p.unit_info[u]);
   const int first = info.x, ns = info.y;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int before = atomicAdd(&p.unit_cnt[u], 1);
-    *last_flag = before == ns - 1;
-  }
-  named_barrier_sync(1, NT);
-  if (!*last_flag) return;
+  const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
   __threadfence();
   const bool tab = MP * ns <= wcap;  // weights fit in shared memory
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // per row: max and weight sum over the pieces (lanes over pieces)
+  // per row: max over the pieces (lanes over pieces), then weights and their sum in order
   for (int r = warp; r < MP; r += NW) {
     float m = -INFINITY;
     for (int s = lane; s < ns; s += 32)
       m = fmaxf(m, __ldcg(p.lse_part + (size_t)piece_slot(first, s) * MP + r));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    float W = 0.f;
-    for (int s = lane; s < ns; s += 32) {
-      const float ls = __ldcg(p.lse_part + (size_t)piece_slot(first, s) * MP + r);
-      const float w = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
-      if (tab) wtab[r * ns + s] = w;
-      W += w;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
+    if (tab)
+      for (int s = lane; s < ns; s += 32) {
+        const float ls = __ldcg(p.lse_part + (size_t)piece_slot(first, s) * MP + r);
+        wtab[r * ns + s] = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+      }
+    __syncwarp();
     if (lane == 0) {
+      float W = 0.f;
+      for (int s = 0; s < ns; ++s) {
+        float w;
+        if (tab) {
+          w = wtab[r * ns + s];
+        } else {
+          const float ls = __ldcg(p.lse_part + (size_t)piece_slot(first, s) * MP + r);
+          w = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+        }
+        W = W + w;
+      }
       stat[2 * r] = m;
       stat[2 * r + 1] = W;
     }
   }
   named_barrier_sync(1, NT);
-  for (int e = threadIdx.x; e < MP * D; e += NT) {
-    const int r = e / D, d = e % D, rg = rb * MP + r;
+  // weighted sum: each thread owns four consecutive head dims of a row
+  for (int e = threadIdx.x; e < MP * D4; e += NT) {
+    const int r = e / D4, d = (e % D4) * 4, rg = rb * MP + r;
     if (rg >= p.M) continue;
     const float m = stat[2 * r], W = stat[2 * r + 1];
-    float O = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     if (W > 0.f) {
 #pragma unroll 4
       for (int s = 0; s < ns; ++s) {
@@ -330,14 +379,49 @@ __device__ __forceinline__ void merge_if_last(const KernelParams& p, int u, int 
           const float ls = __ldcg(p.lse_part + part);
           w = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
         }
-        O += w * __ldcg(p.o_part + part * D + d);
+        if (w == 0.f) continue;  // no key of this row in the piece
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(p.o_part + part * D + d));
+        O.x = __fmaf_rn(w, o.x, O.x);
+        O.y = __fmaf_rn(w, o.y, O.y);
+        O.z = __fmaf_rn(w, o.z, O.z);
+        O.w = __fmaf_rn(w, o.w, O.w);
       }
     }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
     const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
-    store_out<QK>(p.out, row * D + d, W > 0.f ? O / W : 0.f);
+    const float4 v = W > 0.f ? make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    store_out4<QK>(p.out, row * D + d, v);
     if (d == 0 && p.lse) p.lse[row] = W > 0.f ? (m + fast_log2(W)) * kLn2 : -INFINITY;
   }
-  named_barrier_sync(1, NT);  // the shared buffers are reused by the next item
+  if (threadIdx.x == 0) p.unit_cnt[u] = 0;
+  named_barrier_sync(1, NT);  // the shared buffers are reused next
+}
+
+// Publish the partial of the piece in `slot` (every thread's partial writes precede this
+// call behind a CTA barrier).  Called by one thread; the add's result is kept, by the slot's
+// parity, in *pend_even / *pend_odd as (unit, pieces published before this one), to be looked
+// at after the CTA's work list (finish_pending).
+__device__ __forceinline__ void publish_piece(const KernelParams& p, int u, int slot,
+                                              int2* pend_even, int2* pend_odd) {
+  const int before = atom_add_acq_rel_gpu(&p.unit_cnt[u], 1);
+  if (slot & 1)
+    *pend_odd = make_int2(u, before);
+  else
+    *pend_even = make_int2(u, before);
+}
+
+// After the work list: merge the units whose publishing add this CTA made last.
+// `pend` is shared memory holding the two (unit, before) pairs, unit -1 for none.
+template <int D, int MP, int QK, int NW>
+__device__ __forceinline__ void finish_pending(const KernelParams& p, const volatile int* pend,
+                                               float* wtab, int wcap, float* stat) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int u = pend[2 * j], before = pend[2 * j + 1];
+    if (u >= 0 && before == __ldg(&p.unit_info[u].y) - 1)
+      merge_unit<D, MP, QK, NW>(p, u, wtab, wcap, stat);
+  }
 }
 
 // Units with no keys at all: padding rows (zero, lse = -inf), spread over the CTAs.

@@ -44,23 +44,26 @@ struct MmaTraits {
   static constexpr int TT = kTileBytes / (D * BPE);          // tokens per stage
   static constexpr int CPT = TT / 16;                        // 16-token chunks per tile
   static constexpr int NSTAGE = 3;
-  static constexpr int NQ = 1;
-  static constexpr int QSLOT = 0;
-  static constexpr bool WITH_Q = false;  // query fragments are read from global memory
+  static constexpr int NB = D / 8;                          // n-blocks of the output
+  static constexpr int MERGE_SLOT_O = WR * NB * 4 * 32 * 4;  // one warp's accumulators
+  static constexpr int MERGE_O = (NW / 2) * MERGE_SLOT_O;    // tree-merge buffer (last stage)
+  static constexpr int ML_BYTES = round_up(cmax((NW / 2) * WR * 4 * 32 * 4, 2 * MP * 4), 128);
   static constexpr int ROWB = 128;       // swizzled slabs of 128 bytes per row
   static constexpr int NSLAB = D * BPE / 128;
   static constexpr int SLAB = TT * ROWB;  // bytes of one slab of a tile
   static constexpr int KTILE = TT * D * BPE;
   static constexpr int STAGE = round_up(2 * KTILE + (TOKS ? 2 * TT * 4 : 0), 1024);
+  // Query fragments are read from global memory at the start of an item (staging them in
+  // shared memory with the item's first tile measured slower: the wait at an item's start is
+  // the copy pipeline refilling, not the query rows).
+  static constexpr bool WITH_Q = false;
+  static constexpr int NQ = 1;
+  static constexpr int QSLOT = 0;
   static constexpr int OFF_Q = NSTAGE * STAGE;
-  static constexpr int NB = D / 8;                          // n-blocks of the output
-  static constexpr int MERGE_SLOT_O = WR * NB * 4 * 32 * 4;  // one warp's accumulators
-  static constexpr int MERGE_O = (NW / 2) * MERGE_SLOT_O;    // tree-merge buffer (last stage)
-  static constexpr int OFF_ML = OFF_Q;                       // merge max/sum + merge stats
-  static constexpr int ML_BYTES = round_up(cmax((NW / 2) * WR * 4 * 32 * 4, 2 * MP * 4), 128);
+  static constexpr int OFF_ML = OFF_Q + NQ * QSLOT;  // merge max/sum + merge stats
   static constexpr int OFF_BAR = round_up(OFF_ML + ML_BYTES, 64);
   static constexpr int NBAR = 2 * NSTAGE + NQ;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 1024;
   static constexpr int CTAS_PER_SM = 2 * (SMEM + 1024) <= 228 * 1024 ? 2 : 1;
   static_assert(D * BPE >= 128 && (D * BPE) % 128 == 0, "whole 128-byte slabs");
   static_assert(MP % (16 * WR) == 0 && NW % RBW == 0, "row blocks");
@@ -146,7 +149,8 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   uint64_t* empty = full + T::NSTAGE;
   uint64_t* qfull = empty + T::NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(qfull + T::NQ);
-  volatile int* last_flag = abort_flag + 1;
+  volatile int* pend = abort_flag + 2;       // [4]: split pieces published, see finish_pending
+  volatile int* cnt_seen_s = abort_flag + 6;  // published pieces of the item's unit, seen late
   float* mlbuf = reinterpret_cast<float*>(smem + T::OFF_ML);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,6 +163,8 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
     }
     mbar_init(&qfull[0], 32);
     *abort_flag = 0;
+    pend[0] = -1;
+    pend[2] = -1;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -179,13 +185,32 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   const float vts = tensor_scale ? __ldg(p.v_scale) : 1.f;
   const float qk_scale = p.qk_scale * kts;
   uint32_t tile_ctr = 0;
+  int2 pend_even = make_int2(-1, 0), pend_odd = make_int2(-1, 0);  // held by thread 32
 
+  // the next item and its sequence's lengths are read one item ahead
+  int4 item_next = it_begin < it_end ? p.items[it_begin] : make_int4(0, 0, 0, -1);
+  int n_next = 0, ql_next = 0;
+  if (it_begin < it_end) {
+    const int bn = item_next.x / (p.Hkv * p.RB);
+    n_next = __ldg(p.ctx + bn);
+    ql_next = __ldg(p.qlens + bn);
+  }
   for (int it = it_begin; it < it_end; ++it) {
-    const int4 item = p.items[it];
+    const int4 item = item_next;
+    const int n = n_next, ql = ql_next;
+    if (it + 1 < it_end) {
+      item_next = p.items[it + 1];
+      const int bn = item_next.x / (p.Hkv * p.RB);
+      n_next = __ldg(p.ctx + bn);
+      ql_next = __ldg(p.qlens + bn);
+    }
     const int u = item.x, t0 = item.y, t1 = item.z, slot = item.w;
     if (t1 <= t0) continue;
     const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
-    const int n = __ldg(p.ctx + b), ql = __ldg(p.qlens + b);
+    // a piece of a split unit the decode merges: who finishes last is decided at the end
+    const int2 uinfo = slot >= 0 ? __ldg(&p.unit_info[u]) : make_int2(0, 1);
+    const bool in_dec = slot >= 0 && uinfo.y <= p.ns_dec;
+    int cnt_seen = -1;
 
     // query fragments of this warp's rows (A operand, row-major 16 x 16 per k-step)
     uint32_t qa[WR][KSTEPS][4];
@@ -194,7 +219,8 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
     for (int w = 0; w < WR; ++w) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int rg = rb * MP + (rblk * WR + w) * 16 + quad + 8 * h;
+        const int rl = (rblk * WR + w) * 16 + quad + 8 * h;  // row within the unit's tile
+        const int rg = rb * MP + rl;
         const bool real = rg < p.M;
         const int i = rg / p.G, gq = rg % p.G;
         lim[w][h] = (real && i < ql) ? (p.causal ? n - ql + i + 1 : n) : 0;
@@ -247,6 +273,8 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
         atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
         *abort_flag = 1;
       }
+      // with the item's last tile, look how many other pieces are published already
+      if (in_dec && k + 1 == ntiles && threadIdx.x == 32) cnt_seen = ld_acquire_gpu(&p.unit_cnt[u]);
       char* st = smem + s * T::STAGE;
       const uint32_t kt = smem_addr(st), vt = smem_addr(st + T::KTILE);
       const float* sks = reinterpret_cast<const float*>(st + 2 * T::KTILE);
@@ -415,7 +443,10 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
 
     // ---- merge the token streams of each row block (tree through the last stage)
     float* obuf = reinterpret_cast<float*>(smem + s_last * T::STAGE);
+    if (threadIdx.x == 32) *cnt_seen_s = cnt_seen;
     named_barrier_sync(1, T::NTHREADS);  // every warp is done reading the last stage
+    // piece 0, when it ends last, combines the published pieces instead of publishing its own
+    const bool fin = in_dec && slot == uinfo.x && *cnt_seen_s == uinfo.y - 1;
 #pragma unroll
     for (int step = 1; step < T::TS; step <<= 1) {
       const bool writer = (ts & (2 * step - 1)) == step;
@@ -474,34 +505,61 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
           const float m = m_run[w][h];
           const int r = (rblk * WR + w) * 16 + quad + 8 * h;  // row within the unit's block
           const int rg = rb * MP + r;
-          const float inv = L > 0.f ? vts / L : 0.f;
-          const float lse2 = L > 0.f ? m + fast_log2(L) : -INFINITY;
+          float inv = L > 0.f ? vts / L : 0.f;
+          float lse2 = L > 0.f ? m + fast_log2(L) : -INFINITY;
+          // output dims of accumulator entries (2h, 2h + 1) of n-block nb: d0(nb), + DSTEP
+          constexpr int DSTEP = T::FP8 ? 2 : 1;
+          auto d0_of = [&](int nb) {
+            return T::FP8 ? (nb >> 1) * 16 + 4 * qi + (nb & 1) : nb * 8 + 2 * qi;
+          };
           if (rg < p.M) {
             const int i = rg / p.G, hq = g * p.G + rg % p.G;
             const size_t orow = ((size_t)b * p.Sq + i) * p.Hq + hq;
+            if (fin) {
+              // this piece (0) merged with pieces 1 .. ns-1, in the arithmetic of merge_unit:
+              // its normalised partial as it would be stored, then fma in piece order
+              float mx = lse2;
+              for (int sp = 1; sp < uinfo.y; ++sp)
+                mx = fmaxf(mx, __ldcg(p.lse_part + (size_t)piece_slot(uinfo.x, sp) * MP + r));
+              const float wown = lse2 == -INFINITY ? 0.f : fast_exp2(lse2 - mx);
+              float W = 0.f + wown;
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) {
+                const float a0 = o[w][nb][2 * h] * inv, a1 = o[w][nb][2 * h + 1] * inv;
+                o[w][nb][2 * h] = wown == 0.f ? 0.f : __fmaf_rn(wown, a0, 0.f);
+                o[w][nb][2 * h + 1] = wown == 0.f ? 0.f : __fmaf_rn(wown, a1, 0.f);
+              }
+              for (int sp = 1; sp < uinfo.y; ++sp) {
+                const size_t part = (size_t)piece_slot(uinfo.x, sp) * MP + r;
+                const float ls = __ldcg(p.lse_part + part);
+                const float ws = ls == -INFINITY ? 0.f : fast_exp2(ls - mx);
+                W = W + ws;
+                if (ws == 0.f) continue;
+                const float* op = p.o_part + part * D;
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                  o[w][nb][2 * h] = __fmaf_rn(ws, __ldcg(op + d0_of(nb)), o[w][nb][2 * h]);
+                  o[w][nb][2 * h + 1] =
+                      __fmaf_rn(ws, __ldcg(op + d0_of(nb) + DSTEP), o[w][nb][2 * h + 1]);
+                }
+              }
+              inv = W > 0.f ? 1.f / W : 0.f;
+              lse2 = W > 0.f ? mx + fast_log2(W) : -INFINITY;
+            }
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-              // output dims of accumulator entries (2h, 2h + 1) of n-block nb
-              int d0;
-              int dstep;
-              if constexpr (T::FP8) {
-                d0 = (nb >> 1) * 16 + 4 * qi + (nb & 1);
-                dstep = 2;
-              } else {
-                d0 = nb * 8 + 2 * qi;
-                dstep = 1;
-              }
+              const int d0 = d0_of(nb);
               const float v0 = o[w][nb][2 * h] * inv, v1 = o[w][nb][2 * h + 1] * inv;
-              if (slot < 0) {
+              if (slot < 0 || fin) {
                 store_out<QK>(p.out, orow * D + d0, v0);
-                store_out<QK>(p.out, orow * D + d0 + dstep, v1);
+                store_out<QK>(p.out, orow * D + d0 + DSTEP, v1);
               } else {
                 p.o_part[((size_t)slot * MP + r) * D + d0] = v0;
-                p.o_part[((size_t)slot * MP + r) * D + d0 + dstep] = v1;
+                p.o_part[((size_t)slot * MP + r) * D + d0 + DSTEP] = v1;
               }
             }
             if (qi == 0) {
-              if (slot < 0) {
+              if (slot < 0 || fin) {
                 if (p.lse) p.lse[orow] = lse2 * kLn2;
               } else {
                 p.lse_part[(size_t)slot * MP + r] = lse2;
@@ -511,14 +569,27 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
         }
       }
     }
-    named_barrier_sync(1, T::NTHREADS);
-    if (slot >= 0 && p.merge_in_decode)
-      merge_if_last<D, MP, QK, T::NW>(p, u, b, g, rb, obuf, T::MERGE_O / 4 > 0 ? T::STAGE / 4 : 0,
-                                      mlbuf, last_flag);
+    named_barrier_sync(1, T::NTHREADS);  // partials written (or the unit finished)
+    if (in_dec && threadIdx.x == 32) {
+      if (fin) {
+        p.unit_cnt[u] = 0;  // every other piece is published: nobody counts this unit again
+      } else {
+        __threadfence();
+        publish_piece(p, u, slot, &pend_even, &pend_odd);
+      }
+    }
     if (lane == 0) mbar_arrive(&empty[s_last]);
   }
-  if (p.merge_in_decode) zero_empty_units<D, MP, QK, T::NTHREADS>(p);
+  if (threadIdx.x == 32) {
+    pend[0] = pend_even.x;
+    pend[1] = pend_even.y;
+    pend[2] = pend_odd.x;
+    pend[3] = pend_odd.y;
+  }
   if (warp == 0) prod.drain();
+  named_barrier_sync(1, T::NTHREADS);  // no copy in flight: stage 0 is free for the merge
+  finish_pending<D, MP, QK, T::NW>(p, pend, reinterpret_cast<float*>(smem), T::STAGE / 4, mlbuf);
+  zero_empty_units<D, MP, QK, T::NTHREADS>(p);
   grid_dependents_launch();
 }
 

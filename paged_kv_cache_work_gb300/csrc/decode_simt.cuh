@@ -68,13 +68,13 @@ struct SimtTraits {
   static constexpr int MERGE_O = NW * MP * D * 4;
   static constexpr int MERGE_ML = 2 * NW * MP * 4;
   static constexpr int OFF_Q = NSTAGE * STAGE;
-  static constexpr int BASE_BYTES = OFF_Q + NQ * QSLOT + MERGE_ML + 64 + (2 * NSTAGE + NQ) * 8 + 16 + 1024;
+  static constexpr int BASE_BYTES = OFF_Q + NQ * QSLOT + MERGE_ML + 64 + (2 * NSTAGE + NQ) * 8 + kFlagBytes + 1024;
   static constexpr bool OWN_MERGE = 2 * (BASE_BYTES + MERGE_O + 1024) <= 228 * 1024;
   static constexpr int OFF_MERGE = OFF_Q + NQ * QSLOT;
   static constexpr int OFF_MERGE_O = OFF_MERGE + MERGE_ML;
   static constexpr int OFF_BAR = round_up(OFF_MERGE_O + (OWN_MERGE ? MERGE_O : 0), 64);
   static constexpr int NBAR = 2 * NSTAGE + NQ;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 1024;  // + alignment slack
   static constexpr int CTAS_PER_SM = 2 * (SMEM + 1024) <= 228 * 1024 ? 2 : 1;
   static_assert(NV <= LPT && LPT <= 32 && 32 % LPT == 0, "row tile vs lanes");
   static_assert(DPL % EPC == 0 && EPC % 2 == 0, "chunking");
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   uint64_t* empty = full + T::NSTAGE;
   uint64_t* qfull = empty + T::NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(qfull + T::NQ);
-  volatile int* last_flag = abort_flag + 1;  // this CTA finished the last piece of a unit
+  volatile int* pend = abort_flag + 2;  // [4]: split pieces published, see finish_pending
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -249,6 +249,8 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
     }
     for (int s = 0; s < T::NQ; ++s) mbar_init(&qfull[s], 32);
     *abort_flag = 0;
+    pend[0] = -1;
+    pend[2] = -1;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   float* mbuf = reinterpret_cast<float*>(smem + T::OFF_MERGE);  // [NW][MP]
   float* lbuf = mbuf + T::NW * MP;                                // [NW][MP]
   uint32_t tile_ctr = 0, items_seen = 0;
+  int2 pend_even = make_int2(-1, 0), pend_odd = make_int2(-1, 0);  // held by thread 32
 
   int4 item_next = it_begin < it_end ? p.items[it_begin] : make_int4(0, 0, 0, -1);
   int n_next = 0, ql_next = 0;
@@ -449,13 +452,25 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
         if (d == 0) p.lse_part[(size_t)slot * MP + r] = lse2;
       }
     }
-    named_barrier_sync(1, T::NTHREADS);
-    if (slot >= 0 && p.merge_in_decode)
-      merge_if_last<D, MP, QK, T::NW>(p, u, b, g, rb, obuf, T::MERGE_O / 4, mbuf, last_flag);
+    named_barrier_sync(1, T::NTHREADS);  // partials written
+    if (slot >= 0 && threadIdx.x == 32 && __ldg(&p.unit_info[u].y) <= p.ns_dec) {
+      __threadfence();
+      publish_piece(p, u, slot, &pend_even, &pend_odd);
+    }
     if (!T::OWN_MERGE && lane == 0) mbar_arrive(&empty[s_last]);
   }
-  if (p.merge_in_decode) zero_empty_units<D, MP, QK, T::NTHREADS>(p);
+  if (threadIdx.x == 32) {
+    pend[0] = pend_even.x;
+    pend[1] = pend_even.y;
+    pend[2] = pend_odd.x;
+    pend[3] = pend_odd.y;
+  }
   if (warp == 0) prod.drain();
+  named_barrier_sync(1, T::NTHREADS);  // no copy in flight: stage 0 is free for the merge
+  finish_pending<D, MP, QK, T::NW>(
+      p, pend, reinterpret_cast<float*>(smem + (T::OWN_MERGE ? T::OFF_MERGE_O : 0)),
+      T::MERGE_O / 4, mbuf);
+  zero_empty_units<D, MP, QK, T::NTHREADS>(p);
   grid_dependents_launch();
 }
 

@@ -36,12 +36,19 @@ struct Variant {
   int ctas;         // persistent grid size C
   int ctas_per_sm;  // decode CTAs resident per SM
   int bpe;          // bytes per cache element
+  int item_cost;    // tokens of work a unit costs on top of its own (a tile multiple)
+  int ns_dec;       // the decode merges a split unit of at most this many pieces itself
+  int sms;          // SMs of the device when the grid was sized from it, else 0
 };
 
 // Largest row tile of the CUDA-core decode kernel.
 constexpr int kSimtMaxRows = 8;
 // Bytes of one K (or V) tile of a stage.
 constexpr int kTileBytes = 16384;
+// Fixed cost of a work item, in tiles of streaming: a CTA that starts a unit pays for the
+// unit's epilogue and for refilling its copy pipeline (about 5 us at the ~22 GB/s one CTA
+// streams, or three tiles of K and V), so the planner counts every unit that long.
+constexpr int kItemCostTiles = 3;
 
 inline int pow2_at_least(int x) {
   int p = 1;
@@ -55,44 +62,62 @@ int mma_ctas_per_sm(int head_dim, int mp, int kvk, bool toks);
 // Largest row tile of the tensor-core decode kernel.
 constexpr int kMmaMaxRows = 64;
 
+// Partials the last CTA of a unit reads in the decode's own merge: one SM pulls them from
+// L2 while the rest of the grid may be idle, so larger merges go to the reduce kernel.
+constexpr int kDecodeMergeFloats = 32768;
+
+// The most pieces of a split unit the decode kernel merges itself (1: none).
+inline int decode_merge_limit(int split_merge, int mp, int head_dim) {
+  if (split_merge == PA_MERGE_IN_DECODE) return 1 << 30;
+  if (split_merge == PA_MERGE_IN_REDUCE) return 1;
+  const int n = kDecodeMergeFloats / (mp * head_dim);
+  return n > 2 ? n : 2;
+}
+
 // Everything but the grid size, which needs the device (see api.cu).
-// Query tiles of more than 8 rows per kv head run on tensor cores (padded to 16, 32 or 64
-// rows; larger groups are cut into 64-row tiles); the tensor-core kernel needs a tile row of
-// at least one 128-byte slab, so a 64-dim fp8 cache stays on the CUDA-core kernel.
+// Every cache whose tile row is at least one 128-byte slab runs on tensor cores, with the
+// query rows of a kv head padded to 16, 32 or 64 (larger groups are cut into 64-row tiles):
+// even a tile of one real row in sixteen costs less there than the CUDA-core arithmetic.
+// A 64-dim fp8 cache (64-byte rows) runs on the CUDA-core kernel, in tiles of up to 8 rows.
 inline Variant make_variant(const pa_config& c) {
   Variant v{};
   v.rows = (c.num_q_heads / c.num_kv_heads) * c.max_q_len;
   v.bpe = c.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
-  v.path = (v.rows > kSimtMaxRows && c.head_dim * v.bpe >= 128) ? 1 : 0;
+  v.path = c.head_dim * v.bpe >= 128 ? 1 : 0;
   if (v.path == 1)
     v.mp = v.rows >= kMmaMaxRows ? kMmaMaxRows : (v.rows <= 16 ? 16 : pow2_at_least(v.rows));
   else
     v.mp = v.rows <= kSimtMaxRows ? pow2_at_least(v.rows) : kSimtMaxRows;
   v.rb = ceil_div(v.rows, v.mp);
   v.tt = kTileBytes / (c.head_dim * v.bpe);
+  v.item_cost = kItemCostTiles * v.tt;
   v.units = c.batch * c.num_kv_heads * v.rb;
   const int kvk = c.kv_dtype == PA_FP8_E4M3 ? 2 : (c.kv_dtype == PA_FP16 ? 1 : 0);
   const bool toks = c.kv_scale_mode == PA_SCALE_PER_TOKEN;
   v.ctas_per_sm = v.path == 1 ? mma_ctas_per_sm(c.head_dim, v.mp, kvk, toks)
                               : simt_ctas_per_sm(c.head_dim, v.mp, kvk, toks);
+  v.ns_dec = decode_merge_limit(c.split_merge, v.mp, c.head_dim);
   v.ctas = 0;
   return v;
 }
 
 // ---------------------------------------------------------------------------------
 // Workspace layout (byte offsets from ws, every section 256-byte aligned).
-//   header     int32[64]: [0] flags, [1] chunk, [2] active CTAs, [3] items
+//   header     int32[64]: [0] flags, [1] chunk, [2] active CTAs, [3] items,
+//                         [4] units left to the reduce kernel
 //   item_off   int32[C + 1]      first work item of each CTA
 //   items      int4[C + units]   (unit, t0, t1, partial slot or -1)
 //   unit_info  int2[units]       (slot of the first piece, number of pieces); piece s > 0
 //                                of a unit sits in slot 2 * (first / 2 + s)
 //   unit_cnt   int32[units]      pieces of each unit finished so far (merge in decode)
+//   red_units  int32[units]      units the reduce kernel merges, in unit order
 //   seq_start  int32[B + 1]      planner scratch for very large batches
 //   seq_len    int32[B]
 //   o_part     f32[2C * mp * D]  normalised partial outputs (CTA c: slots 2c, 2c + 1)
 //   lse_part   f32[2C * mp]      their log2-sum-exp
 struct WsLayout {
-  size_t header, item_off, items, unit_info, unit_cnt, seq_start, seq_len, o_part, lse_part, total;
+  size_t header, item_off, items, unit_info, unit_cnt, red_units, seq_start, seq_len, o_part,
+      lse_part, total;
 };
 
 inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
@@ -109,6 +134,7 @@ inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
   L.items = take(max_items * sizeof(int4));
   L.unit_info = take((size_t)v.units * sizeof(int2));
   L.unit_cnt = take((size_t)v.units * sizeof(int32_t));
+  L.red_units = take((size_t)v.units * sizeof(int32_t));
   L.seq_start = take(((size_t)c.batch + 1) * sizeof(int32_t));
   L.seq_len = take((size_t)c.batch * sizeof(int32_t));
   const size_t slots = 2 * (size_t)v.ctas;
@@ -118,7 +144,7 @@ inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
   return L;
 }
 
-enum HeaderSlot { HDR_FLAGS = 0, HDR_CHUNK = 1, HDR_ACTIVE = 2, HDR_ITEMS = 3 };
+enum HeaderSlot { HDR_FLAGS = 0, HDR_CHUNK = 1, HDR_ACTIVE = 2, HDR_ITEMS = 3, HDR_NRED = 4 };
 
 // Division by a run-time constant d in [1, 2^31) of a dividend n in [0, 2^31) with one
 // multiply-high, add and shift (the round-up multiplier method of Granlund and Montgomery,
@@ -178,7 +204,6 @@ struct DecodeArgs {
   WsLayout L;
   Variant v;
   int q_kind, kv_kind;
-  int merge_in_decode;
 };
 
 // Returns cudaErrorNotSupported when no kernel instance matches.

@@ -4,10 +4,12 @@
 // Changes): metadata is generated on the device for a persistent decode grid sized as SMs x
 // a grid multiplier (default 1, the safe one-grid-per-CU choice), and ranges that a unit
 // does not finish in one piece are merged by a split reducer.  Here every unit (sequence,
-// kv head, row tile) contributes its context length, rounded up to whole tiles, to one
-// concatenated token space; that space is cut into C equal tile-aligned pieces, one per
-// CTA, so every CTA streams the same number of KV bytes.  A piece that crosses unit
-// boundaries becomes several work items, processed by its CTA in order.
+// kv head, row tile) contributes its context length, rounded up to whole tiles, plus a fixed
+// item cost (the time a CTA spends starting and finishing a unit, in tokens of streaming)
+// to one concatenated token space; that space is cut into C equal tile-aligned pieces, one
+// per CTA, so every CTA gets the same time's work.  A piece that crosses unit boundaries
+// becomes several work items, processed by its CTA in order; the item-cost stretch after a
+// unit's tokens holds no work, and a piece (or its part) that falls there gets no item tokens.
 //
 // Only the first and the last item of a piece can be part of a unit cut into several
 // pieces, so CTA c writes at most two partial results, in slots 2c (its first item) and
@@ -16,6 +18,8 @@
 // on per-sequence prefix sums in shared memory.  One CTA does everything; it checks the
 // lengths and, on a bad one, emits an empty work list so the decode kernel touches nothing
 // (the flags word records why).  Block ids are checked by the decode kernel as it reads them.
+// It also lists the split units whose partials are too large for the decode kernel's own
+// merge (more pieces than ns_dec); the reduce kernel merges those.
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -33,9 +37,12 @@ struct PlanParams {
   int4* items;
   int2* unit_info;
   int32_t* unit_cnt;
+  int32_t* red_units;    // units whose pieces the reduce kernel merges
   int32_t* seq_start_g;  // B + 1 ints in the workspace, used when B > kPlanSmemSeqs
   int32_t* seq_len_g;    // B ints
   int batch, max_q_len, num_kv_heads, rb, block_size, max_blocks, tt, ctas, units;
+  int item_cost;   // tokens of the space a unit costs beyond its own (a tile multiple)
+  int ns_dec;      // the decode merges units of at most this many pieces
   int tt_shift;    // log2(tt): tiles are a power of two
   FastDiv ups_div; // units per sequence
 };
@@ -108,13 +115,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   const int flags = s_flags;
   const int ups = p.num_kv_heads * p.rb;  // units per sequence
   auto pad = [&](int len) { return ((len + p.tt - 1) >> p.tt_shift) << p.tt_shift; };
+  // a unit's stretch of the space: its tokens rounded up to tiles, then the item cost
+  auto stride = [&](int len) { return len > 0 ? pad(len) + p.item_cost : 0; };
 
   // 2. start of each sequence's units in the concatenated, tile-padded token space
   int carry = 0, tot = 0;
   for (int base = 0; base < p.batch; base += kPlanThreads) {
     const int b = base + tid;
     int len = 0;
-    if (b < p.batch && flags == 0) len = pad(seq_len[b]) * ups;
+    if (b < p.batch && flags == 0) len = stride(seq_len[b]) * ups;
     const int excl = block_exclusive_scan(len, &tot, sh);
     if (b < p.batch) seq_start[b] = carry + excl;
     carry += tot;
@@ -138,21 +147,30 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   cdiv.m = s_chunk_div[1];
   cdiv.s = s_chunk_div[2];
 
-  // 4. per unit: its pieces and the slot of its first partial (independent per unit)
-  for (int u = tid; u < p.units; u += kPlanThreads) {
+  // 4. per unit: its pieces and the slot of its first partial, and the list of split units
+  //    too large for the decode's own merge
+  int nred = 0;
+  for (int base = 0; base < p.units; base += kPlanThreads) {
+    const int u = base + tid;
     int ns = 0, first = 0;
-    if (flags == 0) {
+    if (u < p.units && flags == 0) {
       const int b = p.ups_div.div(u), k = u - b * ups;
       const int plen = pad(seq_len[b]);
-      const int st = seq_start[b] + k * plen;
+      const int st = seq_start[b] + k * stride(seq_len[b]);
       if (plen > 0) {
         const int c0 = cdiv.div(st);
         ns = cdiv.div(st + plen - 1) - c0 + 1;
         first = 2 * c0 + (c0 * chunk < st ? 1 : 0);  // the last item of CTA c0, or its first
       }
     }
-    p.unit_info[u] = make_int2(first, ns);
-    p.unit_cnt[u] = 0;
+    const int to_reduce = ns > p.ns_dec ? 1 : 0;
+    const int excl = block_exclusive_scan(to_reduce, &tot, sh);
+    if (u < p.units) {
+      p.unit_info[u] = make_int2(first, ns);
+      p.unit_cnt[u] = 0;
+      if (to_reduce) p.red_units[nred + excl] = u;
+    }
+    nred += tot;
   }
 
   // 5. work items, CTA by CTA
@@ -164,7 +182,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       lo = c * chunk;
       hi = min(lo + chunk, T) - 1;
       const int bf = find_seq(seq_start, p.batch, lo), bl = find_seq(seq_start, p.batch, hi);
-      const int pf = pad(seq_len[bf]), pl = pad(seq_len[bl]);
+      const int pf = stride(seq_len[bf]), pl = stride(seq_len[bl]);
       uf = bf * ups + (lo - seq_start[bf]) / pf;
       const int ul = bl * ups + (hi - seq_start[bl]) / pl;
       cnt = ul - uf + 1;
@@ -176,12 +194,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       const int b = p.ups_div.div(u), ku = u - b * ups;
       const int len = seq_len[b];
       const int plen = pad(len);
-      const int st = seq_start[b] + ku * plen;
+      const int st = seq_start[b] + ku * stride(len);
       int t0 = 0, t1 = 0, slot = -1;
       if (plen > 0) {
         t0 = max(lo, st) - st;
         t1 = min(hi + 1 - st, len);
-        if (cdiv.div(st + plen - 1) != cdiv.div(st)) slot = 2 * c + (k > 0 ? 1 : 0);
+        if (t1 <= t0) {
+          t0 = t1 = 0;  // only the item-cost stretch of the unit lies in this piece
+        } else if (cdiv.div(st + plen - 1) != cdiv.div(st)) {
+          slot = 2 * c + (k > 0 ? 1 : 0);
+        }
       }
       p.items[carry + excl + k] = make_int4(u, t0, t1, slot);
     }
@@ -193,6 +215,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     p.hdr[HDR_CHUNK] = chunk;
     p.hdr[HDR_ACTIVE] = active;
     p.hdr[HDR_ITEMS] = carry;
+    p.hdr[HDR_NRED] = nred;
   }
 }
 
@@ -208,6 +231,7 @@ cudaError_t launch_plan(const ProblemArgs& a, const Variant& v, const WsLayout& 
   p.items = reinterpret_cast<int4*>(ws + L.items);
   p.unit_info = reinterpret_cast<int2*>(ws + L.unit_info);
   p.unit_cnt = reinterpret_cast<int32_t*>(ws + L.unit_cnt);
+  p.red_units = reinterpret_cast<int32_t*>(ws + L.red_units);
   p.seq_start_g = reinterpret_cast<int32_t*>(ws + L.seq_start);
   p.seq_len_g = reinterpret_cast<int32_t*>(ws + L.seq_len);
   p.batch = a.batch;
@@ -217,8 +241,10 @@ cudaError_t launch_plan(const ProblemArgs& a, const Variant& v, const WsLayout& 
   p.block_size = a.block_size;
   p.max_blocks = a.max_blocks;
   p.tt = v.tt;
+  p.item_cost = v.item_cost;
   p.ctas = v.ctas;
   p.units = v.units;
+  p.ns_dec = v.ns_dec;
   p.tt_shift = ilog2((uint32_t)v.tt);
   p.ups_div = FastDiv((uint32_t)(a.num_kv_heads * v.rb));
   cudaLaunchConfig_t cfg = {};

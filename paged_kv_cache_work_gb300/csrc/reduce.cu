@@ -69,7 +69,7 @@ KernelParams make_kernel_params(const DecodeArgs& a) {
   p.unit_info = reinterpret_cast<const int2*>(a.ws + a.L.unit_info);
   p.unit_cnt = reinterpret_cast<int32_t*>(a.ws + a.L.unit_cnt);
   p.units = a.v.units;
-  p.merge_in_decode = a.merge_in_decode;
+  p.ns_dec = a.v.ns_dec;
   p.scale_mode = a.scale_mode;
   p.Sq = a.p.max_q_len;
   p.Hq = a.p.num_q_heads;
@@ -111,65 +111,145 @@ namespace {
 struct ReduceParams {
   void* out;
   float* lse;
+  const int32_t* hdr;
+  const int32_t* red_units;
   const int2* unit_info;
   const float* o_part;
   const float* lse_part;
-  int Sq, Hq, Hkv, G, M, RB, MP, D;
-  int q_kind;
+  int Sq, Hq, Hkv, G, M, RB, MP;
 };
 
-constexpr int kReduceWarps = 4;
+constexpr int kReduceWarps = 8;
 
-// One CTA per unit; warp w merges rows w, w + 4, ...: the lanes share the splits for the
-// max and the weight sum, then the head dimensions for the weighted sum of the partials.
+// One CTA per (listed unit, row): warp w folds pieces w, w + 8, ... into a running
+// (max, weight sum, weighted sum) with lanes over the head dimension, four floats a lane,
+// loading the partials of four pieces at a time; the eight warps' results are then combined
+// in shared memory.  Rows of all listed units are spread over the grid, so a unit cut into
+// many pieces is merged by many SMs at once.  Every sum runs in a fixed order.
+template <int D, int QK>
 __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p) {
+  constexpr int D4 = D / 4;
+  constexpr int NV = (D4 + 31) / 32;  // float4 columns per lane
+  __shared__ float s_m[kReduceWarps], s_w[kReduceWarps];
+  __shared__ float4 s_acc[kReduceWarps][D4];
   grid_dependency_wait();  // partials come from the decode kernel launched just before
-  const int u = blockIdx.x;
-  const int2 info = p.unit_info[u];
-  if (info.y != 1) {
-    const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int r = warp; r < p.MP; r += kReduceWarps) {
-      const int rg = rb * p.MP + r;
-      if (rg >= p.M) continue;
-      const int i = rg / p.G, h = g * p.G + rg % p.G;
-      const size_t row = ((size_t)b * p.Sq + i) * p.Hq + h;
-      float m = -INFINITY;
-      for (int s = lane; s < info.y; s += 32)
-        m = fmaxf(m, p.lse_part[(size_t)piece_slot(info.x, s) * p.MP + r]);
+  const int nred = p.hdr[HDR_NRED];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int w = blockIdx.x; w < nred * p.MP; w += gridDim.x) {
+    const int u = p.red_units[w / p.MP], r = w % p.MP;
+    const int rb = u % p.RB, rg = rb * p.MP + r;
+    if (rg >= p.M) continue;  // uniform over the CTA
+    const int2 info = p.unit_info[u];
+    float m = -INFINITY, W = 0.f;
+    float4 acc[NV];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-      float W = 0.f;
-      if (m != -INFINITY) {
-        for (int s = lane; s < info.y; s += 32) {
-          const float ls = p.lse_part[(size_t)piece_slot(info.x, s) * p.MP + r];
-          W += ls == -INFINITY ? 0.f : fast_exp2(ls - m);
-        }
+    for (int v = 0; v < NV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // batches of up to 32 pieces per warp: lane j holds the weight of piece s0 + 8 j
+    for (int s0 = warp; s0 < info.y; s0 += 32 * kReduceWarps) {
+      const int sl = s0 + lane * kReduceWarps;
+      const float ls = sl < info.y ? p.lse_part[(size_t)piece_slot(info.x, sl) * p.MP + r]
+                                   : -INFINITY;
+      float mb = ls;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
+      for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+      if (mb == -INFINITY) continue;  // no key of this row in the batch (uniform)
+      const float mn = fmaxf(m, mb);
+      const float sc = m == -INFINITY ? 0.f : fast_exp2(m - mn);
+      m = mn;
+      W *= sc;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        acc[v].x *= sc;
+        acc[v].y *= sc;
+        acc[v].z *= sc;
+        acc[v].w *= sc;
       }
-      const float inv = W > 0.f ? 1.f / W : 0.f;
-      for (int d = lane; d < p.D; d += 32) {
-        float O = 0.f;
-        if (W > 0.f) {
-#pragma unroll 4
-          for (int s = 0; s < info.y; ++s) {
-            const size_t part = (size_t)piece_slot(info.x, s) * p.MP + r;
-            const float ls = p.lse_part[part];
-            const float w = ls == -INFINITY ? 0.f : fast_exp2(ls - m);
-            O += w * p.o_part[part * p.D + d];
+      const float wl = ls == -INFINITY ? 0.f : fast_exp2(ls - m);
+      float wsum = wl;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(kFull, wsum, o);
+      W += wsum;
+      const int cnt = min(32, (info.y - s0 + kReduceWarps - 1) / kReduceWarps);
+      for (int j0 = 0; j0 < cnt; j0 += 4) {
+        float wj[4];
+        float4 o[4][NV];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          wj[jj] = __shfl_sync(kFull, wl, (j0 + jj) & 31);
+          const bool ok = j0 + jj < cnt;
+          const size_t part = ok ? (size_t)piece_slot(info.x, s0 + (j0 + jj) * kReduceWarps) * p.MP + r : 0;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            const int c = lane + 32 * v;
+            o[jj][v] = (ok && c < D4) ? reinterpret_cast<const float4*>(p.o_part + part * D)[c]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
-        const float val = O * inv;
-        if (p.q_kind == Q_BF16)
-          reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.D + d] = __float2bfloat16_rn(val);
-        else
-          reinterpret_cast<__half*>(p.out)[row * p.D + d] = __float2half_rn(val);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const float x = j0 + jj < cnt ? wj[jj] : 0.f;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            acc[v].x += x * o[jj][v].x;
+            acc[v].y += x * o[jj][v].y;
+            acc[v].z += x * o[jj][v].z;
+            acc[v].w += x * o[jj][v].w;
+          }
+        }
       }
-      if (lane == 0 && p.lse) p.lse[row] = W > 0.f ? (m + fast_log2(W)) * kLn2 : -INFINITY;
     }
+    if (lane == 0) {
+      s_m[warp] = m;
+      s_w[warp] = W;
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+      if (lane + 32 * v < D4) s_acc[warp][lane + 32 * v] = acc[v];
+    __syncthreads();
+    float mt = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kReduceWarps; ++k) mt = fmaxf(mt, s_m[k]);
+    float Wt = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int c = threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < kReduceWarps; ++k) {
+      if (s_m[k] == -INFINITY) continue;
+      const float sc = fast_exp2(s_m[k] - mt);
+      Wt += sc * s_w[k];
+      if (c < D4) {
+        const float4 a = s_acc[k][c];
+        O.x += sc * a.x;
+        O.y += sc * a.y;
+        O.z += sc * a.z;
+        O.w += sc * a.w;
+      }
+    }
+    const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv;
+    const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
+    if (c < D4) {
+      const float inv = Wt > 0.f ? 1.f / Wt : 0.f;
+      store_out4<QK>(p.out, row * D + 4 * c, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+    }
+    if (c == 0 && p.lse) p.lse[row] = Wt > 0.f ? (mt + fast_log2(Wt)) * kLn2 : -INFINITY;
+    __syncthreads();  // shared results are rewritten by the next row
   }
   grid_dependents_launch();
+}
+
+template <int D>
+cudaError_t launch_reduce_d(const ReduceParams& p, int q_kind, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kReduceWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (q_kind == Q_BF16) return cudaLaunchKernelEx(&cfg, reduce_kernel<D, Q_BF16>, p);
+  return cudaLaunchKernelEx(&cfg, reduce_kernel<D, Q_FP16>, p);
 }
 
 }  // namespace
@@ -178,6 +258,8 @@ cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s) {
   ReduceParams p;
   p.out = a.out;
   p.lse = a.lse;
+  p.hdr = reinterpret_cast<const int32_t*>(a.ws + a.L.header);
+  p.red_units = reinterpret_cast<const int32_t*>(a.ws + a.L.red_units);
   p.unit_info = reinterpret_cast<const int2*>(a.ws + a.L.unit_info);
   p.o_part = reinterpret_cast<const float*>(a.ws + a.L.o_part);
   p.lse_part = reinterpret_cast<const float*>(a.ws + a.L.lse_part);
@@ -188,19 +270,23 @@ cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s) {
   p.M = a.v.rows;
   p.RB = a.v.rb;
   p.MP = a.v.mp;
-  p.D = a.p.head_dim;
-  p.q_kind = a.q_kind;
   if (a.v.units == 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.v.units);
-  cfg.blockDim = dim3(kReduceWarps * 32);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, reduce_kernel, p);
+  // (unit, row) pairs never exceed units x mp; eight CTAs per SM cover them in a few rounds
+  int sms = a.v.sms;
+  if (sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cudaErrorUnknown;
+  }
+  const long long pairs = (long long)a.v.units * a.v.mp;
+  const int grid = (int)(pairs < 8LL * sms ? pairs : 8LL * sms);
+  switch (a.p.head_dim) {
+    case 64: return launch_reduce_d<64>(p, a.q_kind, grid, s);
+    case 128: return launch_reduce_d<128>(p, a.q_kind, grid, s);
+    case 256: return launch_reduce_d<256>(p, a.q_kind, grid, s);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace pa

@@ -17,7 +17,7 @@ LSE_TOL = 2e-4
 
 
 def run(inp_dev: dict, num_ctas: int = 0, grid_mult: int = 0, with_lse: bool = True,
-        split_merge: int = pa.MERGE_IN_DECODE):
+        split_merge: int = pa.MERGE_AUTO):
     cfg = pa.config_for(inp_dev, num_ctas=num_ctas, grid_mult=grid_mult, split_merge=split_merge)
     q = inp_dev["q"]
     out = torch.full_like(q, float("nan"))
@@ -66,19 +66,31 @@ def _pow2_at_least(x):
 
 SIMT_MAX_ROWS = 8
 TILE_BYTES = 16384
+ITEM_COST_TILES = 3
+DECODE_MERGE_FLOATS = 32768
+
+
+def decode_merge_limit(split_merge: int, mp: int, head_dim: int) -> int:
+    """Most pieces of a split unit that the decode kernel merges itself (pa_split_merge)."""
+    if split_merge == pa.MERGE_IN_DECODE:
+        return 1 << 30
+    if split_merge == pa.MERGE_IN_REDUCE:
+        return 1
+    return max(2, DECODE_MERGE_FLOATS // (mp * head_dim))
 
 
 def variant(cfg: pa.PaConfig, ctas: int):
     rows = (cfg.num_q_heads // cfg.num_kv_heads) * cfg.max_q_len
     bpe = 1 if cfg.kv_dtype == pa.FP8_E4M3 else 2
-    if rows > SIMT_MAX_ROWS and cfg.head_dim * bpe >= 128:  # tensor-core kernel
+    if cfg.head_dim * bpe >= 128:  # tensor-core kernel
         mp = 64 if rows >= 64 else (16 if rows <= 16 else _pow2_at_least(rows))
     else:
         mp = _pow2_at_least(rows) if rows <= SIMT_MAX_ROWS else SIMT_MAX_ROWS
     rb = -(-rows // mp)
     tt = TILE_BYTES // (cfg.head_dim * bpe)
     return dict(rows=rows, mp=mp, rb=rb, tt=tt, units=cfg.batch * cfg.num_kv_heads * rb,
-                ctas=ctas)
+                ctas=ctas, ns_dec=decode_merge_limit(cfg.split_merge, mp, cfg.head_dim),
+                item_cost=ITEM_COST_TILES * tt)
 
 
 def layout(cfg: pa.PaConfig, v: dict):
@@ -96,6 +108,7 @@ def layout(cfg: pa.PaConfig, v: dict):
     take("items", (C + U) * 16)
     take("unit_info", U * 8)
     take("unit_cnt", U * 4)
+    take("red_units", U * 4)
     take("seq_start", (cfg.batch + 1) * 4)
     take("seq_len", cfg.batch * 4)
     take("o_part", 2 * C * v["mp"] * cfg.head_dim * 4)
@@ -119,12 +132,16 @@ def plan_view(ws: torch.Tensor, cfg: pa.PaConfig, ctas: int):
     item_off = arr("item_off", np.int32, C + 1)
     items = arr("items", np.int32, 4 * (C + U)).reshape(-1, 4)
     unit_info = arr("unit_info", np.int32, 2 * U).reshape(-1, 2)
+    unit_cnt = arr("unit_cnt", np.int32, U)
+    n_red = int(hdr[4])
+    red_units = arr("red_units", np.int32, U)[:n_red]
     o_part = arr("o_part", np.float32, 2 * C * v["mp"] * cfg.head_dim).reshape(
         2 * C, v["mp"], cfg.head_dim)
     lse_part = arr("lse_part", np.float32, 2 * C * v["mp"]).reshape(2 * C, v["mp"])
     return dict(v=v, flags=int(hdr[0]), chunk=int(hdr[1]), active=int(hdr[2]),
                 n_items=int(hdr[3]), item_off=item_off.copy(), items=items.copy(),
-                unit_info=unit_info.copy(), o_part=o_part.copy(), lse_part=lse_part.copy())
+                unit_info=unit_info.copy(), unit_cnt=unit_cnt.copy(), red_units=red_units.copy(),
+                o_part=o_part.copy(), lse_part=lse_part.copy())
 
 
 def sample_rows(w: workloads.Workload, ql, n: int, seed: int):

@@ -98,6 +98,8 @@ def test_workspace_grows_with_grid_and_batch(lib):
     (dict(q_dtype=7), pa.ERR_INVALID_ARG),
     (dict(kv_scale_mode=5), pa.ERR_INVALID_ARG),
     (dict(num_ctas=-1), pa.ERR_INVALID_ARG),
+    (dict(split_merge=3), pa.ERR_INVALID_ARG),
+    (dict(split_merge=-1), pa.ERR_INVALID_ARG),
 ])
 def test_rejections(lib, kw, expect):
     st, _ = ws_size(lib, base_cfg(**kw))

@@ -46,3 +46,29 @@ def test_eager_repeat_and_graph_replay_bitwise(wl, cuda_device):
     assert torch.equal(outs[0][0].view(torch.int16), g_out.view(torch.int16))
     assert torch.equal(outs[0][1].view(torch.int32), g_lse.view(torch.int32))
     assert pa.read_flags(ws) == 0
+
+
+@pytest.mark.parametrize("mode", ["auto", "in_decode", "in_reduce"])
+@pytest.mark.parametrize("wl", CASES[:2], ids=lambda w: w.name)
+def test_decode_repeats_on_one_plan(wl, mode, cuda_device):
+    """pa_plan once, then decode + reduce twice: the merge counters the last CTA of each unit
+    sets back to zero let the second decode merge exactly like the first."""
+    sm = {"auto": pa.MERGE_AUTO, "in_decode": pa.MERGE_IN_DECODE,
+          "in_reduce": pa.MERGE_IN_REDUCE}[mode]
+    inp = W.make_inputs(wl, 2029, device=cuda_device)
+    cfg = pa.config_for(inp, split_merge=sm)
+    q = inp["q"]
+    ws = torch.empty(pa.workspace_size(cfg), dtype=torch.uint8, device=cuda_device)
+    pa.plan(cfg, inp["block_tables"], inp["context_lens"], inp["q_lens"], ws)
+    outs = []
+    for _ in range(2):
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=cuda_device)
+        pa.decode(cfg, q, inp["k_cache"], inp["v_cache"], inp["k_scale"], inp["v_scale"],
+                  inp["block_tables"], inp["context_lens"], inp["q_lens"], out, lse, ws)
+        pa.reduce(cfg, out, lse, ws)
+        outs.append((out, lse))
+    torch.cuda.synchronize()
+    assert not torch.isnan(outs[0][0]).any()
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int32), outs[1][1].view(torch.int32))

@@ -123,7 +123,7 @@ EDGE = [
                             block_size=16, ctx=[257, 900])),
     ("rows_3_padded", dict(batch=2, max_q_len=3, num_q_heads=2, num_kv_heads=2, head_dim=256,
                            block_size=32, ctx=[100, 64], causal=True)),
-    # tensor-core kernel (more than 8 query rows per kv head)
+    # tensor-core kernel: row tiles of 16, 32 and 64
     ("mma_rows12_padded", dict(batch=3, max_q_len=1, num_q_heads=24, num_kv_heads=2,
                                head_dim=128, block_size=16, ctx=[77, 300, 16])),
     ("mma_rows100_two_tiles", dict(batch=2, max_q_len=4, num_q_heads=25, num_kv_heads=1,
@@ -159,6 +159,37 @@ def test_edge_cases(name, kw, cuda_device, pa):
     assert pa.read_flags(ws) == 0
 
 
+# The CUDA-core kernel serves caches whose rows are shorter than one 128-byte slab: 64-dim fp8.
+CUDA_CORE = [
+    ("rows1_tensor", dict(batch=3, max_q_len=1, num_q_heads=4, num_kv_heads=4, block_size=16,
+                          ctx=[300, 17, 1200], scale_mode="tensor")),
+    ("rows2_token_causal", dict(batch=2, max_q_len=2, num_q_heads=2, num_kv_heads=2,
+                                block_size=32, ctx=[129, 640], scale_mode="token", causal=True)),
+    ("rows4_none", dict(batch=4, max_q_len=1, num_q_heads=8, num_kv_heads=2, block_size=64,
+                        ctx=[1, 64, 65, 2000], scale_mode="none")),
+    ("rows8_fp16q", dict(batch=2, max_q_len=2, num_q_heads=8, num_kv_heads=2, block_size=128,
+                         ctx=[700, 260], scale_mode="token", q_dtype="fp16", causal=True)),
+    ("rows12_two_tiles", dict(batch=2, max_q_len=3, num_q_heads=4, num_kv_heads=1,
+                              block_size=16, ctx=[90, 333], q_lens=[3, 2], scale_mode="tensor",
+                              causal=True)),
+    ("empty_and_ragged", dict(batch=3, max_q_len=4, num_q_heads=2, num_kv_heads=1,
+                              block_size=16, ctx=[0, 5, 77], q_lens=[0, 4, 1],
+                              scale_mode="token", causal=True)),
+]
+
+
+@pytest.mark.parametrize("ctas", [0, 5])
+@pytest.mark.parametrize("name,kw", CUDA_CORE, ids=[c[0] for c in CUDA_CORE])
+def test_cuda_core_kernel(name, kw, ctas, cuda_device, pa):
+    rng = np.random.default_rng(abs(hash(name)) % (1 << 31) + ctas)
+    inp, _ = random_problem(rng, head_dim=64, kv_dtype="fp8", **kw)
+    ref_out, ref_lse = oracle.decode(inp, "f32")
+    for sm in (pa.MERGE_AUTO, pa.MERGE_IN_DECODE, pa.MERGE_IN_REDUCE):
+        out, lse, ws, _ = run(W.to_device(inp, cuda_device), num_ctas=ctas, split_merge=sm)
+        compare(out, lse, ref_out, ref_lse, "fp8")
+        assert pa.read_flags(ws) == 0
+
+
 @pytest.mark.parametrize("bs", [16, 32, 64, 128, 256, 512, 1024])
 def test_every_page_size(bs, cuda_device, pa):
     rng = np.random.default_rng(bs)
@@ -189,14 +220,15 @@ MERGE_CASES = [W.reduced(W.GQA_B32, 5, 300, 1400), W.reduced(W.LONG_SQ4, 2, 2500
                W.reduced(W.FP8_TOKEN_SQ4, 3, 1100, 3000), W.reduced(W.mha_d256(8, 16), 2, 200, 1300)]
 
 
+@pytest.mark.parametrize("mode", ["in_reduce", "in_decode"])
 @pytest.mark.parametrize("ctas", [0, 40])
 @pytest.mark.parametrize("wl", MERGE_CASES, ids=lambda w: w.name)
-def test_split_merge_in_reduce_kernel(wl, ctas, cuda_device, pa):
-    """The standalone reducer (PA_MERGE_IN_REDUCE) against the oracle."""
+def test_split_merge_modes(wl, ctas, mode, cuda_device, pa):
+    """Every split merged by the reduce kernel, or every one by the decode's last CTA."""
     inp = W.make_inputs(wl, 2039)
     ref_out, ref_lse = oracle.decode(inp, "f32")
-    out, lse, ws, _ = run(W.to_device(inp, cuda_device), num_ctas=ctas,
-                          split_merge=pa.MERGE_IN_REDUCE)
+    sm = pa.MERGE_IN_REDUCE if mode == "in_reduce" else pa.MERGE_IN_DECODE
+    out, lse, ws, _ = run(W.to_device(inp, cuda_device), num_ctas=ctas, split_merge=sm)
     compare(out, lse, ref_out, ref_lse, wl.kv_dtype)
     assert pa.read_flags(ws) == 0
 

@@ -2,11 +2,14 @@
 
 * bit-exact coverage: every (sequence, kv head, row tile, token) lies in exactly one work
   item, and items never reach past a sequence's context;
-* every CTA's piece is contiguous in the concatenated tile-padded token space and no
-  longer than the chunk, and the chunk is the smallest tile multiple that fits the work
-  in C pieces;
+* every CTA's items are exactly the units its piece of the concatenated token space
+  overlaps (each unit its tile-padded length plus a fixed item cost), with the token range
+  the piece holds, and the chunk is the smallest tile multiple that fits the space in C
+  pieces;
 * the partial slots of units cut into several pieces are CTA c's slots 2c / 2c + 1, and
   the unit table points at them;
+* the reduce list holds exactly the units of more pieces than the decode merges itself, in
+  unit order, and a finished decode leaves every merge counter at zero;
 * each partial the decode kernel wrote equals the oracle's attention over that item's
   key range (so the split mode is checked on its own, before the reducer).
 """
@@ -23,13 +26,16 @@ pytestmark = pytest.mark.gpu
 
 
 def check_plan(view, ctx, ctas, hkv):
-    """Exact checks of the work list against the cutting rule stated in pa.h."""
+    """Exact checks of the work list against the cutting rule stated in plan.cu: units laid
+    end to end, each its tile-padded length plus the fixed item cost (none for an empty
+    unit), the space cut into equal tile-aligned pieces, one per CTA."""
     v = view["v"]
-    tt, U, rb = v["tt"], v["units"], v["rb"]
+    tt, U, rb, cost = v["tt"], v["units"], v["rb"], v["item_cost"]
     per_seq = hkv * rb
     lens = np.array([ctx[u // per_seq] for u in range(U)], np.int64)
     plen = -(-lens // tt) * tt
-    start = np.concatenate([[0], np.cumsum(plen)])
+    stride = np.where(lens > 0, plen + cost, 0)
+    start = np.concatenate([[0], np.cumsum(stride)])
     T = int(start[-1])
     chunk = view["chunk"]
     if T > 0:
@@ -43,30 +49,29 @@ def check_plan(view, ctx, ctas, hkv):
     covered = [np.zeros(int(n), np.int32) for n in lens]
     slots = {}
     for c in range(ctas):
-        active = c < view["active"]
-        lo = c * chunk
-        hi = min(lo + chunk, T) if active else lo
-        pos = lo
-        n_c = item_off[c + 1] - item_off[c]
-        for k, it in enumerate(range(item_off[c], item_off[c + 1])):
-            u, t0, t1, slot = (int(x) for x in items[it])
-            assert active and 0 <= u < U
+        got = [tuple(int(x) for x in items[it]) for it in range(item_off[c], item_off[c + 1])]
+        want = []
+        if c < view["active"]:
+            lo, hi = c * chunk, min((c + 1) * chunk, T)
+            for u in range(U):
+                st = int(start[u])
+                if stride[u] == 0 or st >= hi or st + stride[u] <= lo:
+                    continue
+                t0, t1 = max(lo, st) - st, min(hi - st, int(lens[u]))
+                if t1 <= t0:
+                    want.append((u, 0, 0, -1))  # only the unit's item-cost stretch
+                    continue
+                split = (st + plen[u] - 1) // chunk != st // chunk
+                want.append((u, t0, t1, 2 * c + (1 if want else 0) if split else -1))
+        assert got == want, f"CTA {c}: {got} != {want}"
+        for k, (u, t0, t1, slot) in enumerate(got):
             if t1 <= t0:
-                assert lens[u] == 0
                 continue
-            assert 0 <= t0 < t1 <= lens[u] and t0 % tt == 0
-            assert start[u] + t0 == pos, "piece not contiguous"
-            if t1 < lens[u]:
-                assert t1 % tt == 0
-                pos = start[u] + t1
-            else:
-                pos = start[u] + plen[u]
+            assert t0 % tt == 0 and (t1 % tt == 0 or t1 == lens[u])
             covered[u][t0:t1] += 1
             slots.setdefault(u, []).append(slot)
             if slot >= 0:  # only a piece's first or last item can be split
-                assert slot == 2 * c + (1 if k > 0 else 0)
-                assert k == 0 or k == n_c - 1
-        assert pos == hi, "piece does not end where the next begins"
+                assert k == 0 or k == len(got) - 1
     for u in range(U):
         assert (covered[u] == 1).all(), f"unit {u} not covered exactly once"
         info = view["unit_info"][u]
@@ -77,6 +82,9 @@ def check_plan(view, ctx, ctas, hkv):
         elif ns > 1:
             first = int(info[0])
             assert slots[u] == [first] + [2 * (first // 2 + s) for s in range(1, ns)]
+    want_red = [u for u in range(U) if int(view["unit_info"][u][1]) > v["ns_dec"]]
+    assert view["red_units"].tolist() == want_red
+    assert (view["unit_cnt"] == 0).all(), "merge counters not reset by the decode"
     return T
 
 
@@ -94,10 +102,11 @@ def test_work_list_covers_every_token_once(name, wl, grids, cuda_device, pa):
         inp = W.make_inputs(wl, seed, device=cuda_device)
         ctx = inp["context_lens"].cpu().numpy()
         for ctas in grids:
-            _, _, ws, cfg = run(inp, num_ctas=ctas)
-            view = plan_view(ws, cfg, ctas)
-            assert view["flags"] == 0
-            check_plan(view, ctx, ctas, wl.num_kv_heads)
+            for sm in (pa.MERGE_AUTO, pa.MERGE_IN_DECODE, pa.MERGE_IN_REDUCE):
+                _, _, ws, cfg = run(inp, num_ctas=ctas, split_merge=sm)
+                view = plan_view(ws, cfg, ctas)
+                assert view["flags"] == 0
+                check_plan(view, ctx, ctas, wl.num_kv_heads)
 
 
 def test_random_shapes_coverage(cuda_device, pa):
