@@ -197,8 +197,8 @@ pa_status pa_decode(const pa_config* cfg, const void* q, const void* k_cache, co
 
   const int box_rows = cfg->block_size < v.tt ? cfg->block_size : v.tt;
   CUtensorMap kmap, vmap;
-  if (!kv_tensor_map(&kmap, k_cache, *cfg, box_rows, v.path == 1) ||
-      !kv_tensor_map(&vmap, v_cache, *cfg, box_rows, v.path == 1))
+  if (!kv_tensor_map(&kmap, k_cache, *cfg, box_rows, v.path >= 1) ||
+      !kv_tensor_map(&vmap, v_cache, *cfg, box_rows, v.path >= 1))
     return PA_ERR_CUDA;
 
   DecodeArgs a;

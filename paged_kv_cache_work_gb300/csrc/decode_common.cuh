@@ -321,9 +321,10 @@ __device__ __forceinline__ int piece_index(int first, int slot) {
 
 // Merge every published piece of unit u with the log-sum-exp rule and write its output
 // rows, then reset its count.  All NW warps of the CTA take part.
+// `tid` numbers the NW warps that take part from 0 (they use named barrier 1).
 template <int D, int MP, int QK, int NW>
 __device__ __forceinline__ void merge_unit(const KernelParams& p, int u, float* wtab, int wcap,
-                                           float* stat) {
+                                           float* stat, int tid) {
   constexpr int NT = NW * 32;
   constexpr int D4 = D / 4;
   const int2 info = __ldg(&p.unit_info[u]);
@@ -331,7 +332,7 @@ __device__ __forceinline__ void merge_unit(const KernelParams& p, int u, float* 
   const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
   __threadfence();
   const bool tab = MP * ns <= wcap;  // weights fit in shared memory
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = tid >> 5, lane = tid & 31;
   // per row: max over the pieces (lanes over pieces), then weights and their sum in order
   for (int r = warp; r < MP; r += NW) {
     float m = -INFINITY;
@@ -363,7 +364,7 @@ __device__ __forceinline__ void merge_unit(const KernelParams& p, int u, float* 
   }
   named_barrier_sync(1, NT);
   // weighted sum: each thread owns four consecutive head dims of a row
-  for (int e = threadIdx.x; e < MP * D4; e += NT) {
+  for (int e = tid; e < MP * D4; e += NT) {
     const int r = e / D4, d = (e % D4) * 4, rg = rb * MP + r;
     if (rg >= p.M) continue;
     const float m = stat[2 * r], W = stat[2 * r + 1];
@@ -394,7 +395,7 @@ __device__ __forceinline__ void merge_unit(const KernelParams& p, int u, float* 
     store_out4<QK>(p.out, row * D + d, v);
     if (d == 0 && p.lse) p.lse[row] = W > 0.f ? (m + fast_log2(W)) * kLn2 : -INFINITY;
   }
-  if (threadIdx.x == 0) p.unit_cnt[u] = 0;
+  if (tid == 0) p.unit_cnt[u] = 0;
   named_barrier_sync(1, NT);  // the shared buffers are reused next
 }
 
@@ -415,22 +416,23 @@ __device__ __forceinline__ void publish_piece(const KernelParams& p, int u, int 
 // `pend` is shared memory holding the two (unit, before) pairs, unit -1 for none.
 template <int D, int MP, int QK, int NW>
 __device__ __forceinline__ void finish_pending(const KernelParams& p, const volatile int* pend,
-                                               float* wtab, int wcap, float* stat) {
+                                               float* wtab, int wcap, float* stat,
+                                               int tid = threadIdx.x) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int u = pend[2 * j], before = pend[2 * j + 1];
     if (u >= 0 && before == __ldg(&p.unit_info[u].y) - 1)
-      merge_unit<D, MP, QK, NW>(p, u, wtab, wcap, stat);
+      merge_unit<D, MP, QK, NW>(p, u, wtab, wcap, stat, tid);
   }
 }
 
 // Units with no keys at all: padding rows (zero, lse = -inf), spread over the CTAs.
 template <int D, int MP, int QK, int NT>
-__device__ __forceinline__ void zero_empty_units(const KernelParams& p) {
+__device__ __forceinline__ void zero_empty_units(const KernelParams& p, int tid = threadIdx.x) {
   for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
     if (__ldg(&p.unit_info[u].y) != 0) continue;
     const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv, rb = u % p.RB;
-    for (int e = threadIdx.x; e < MP * D; e += NT) {
+    for (int e = tid; e < MP * D; e += NT) {
       const int r = e / D, d = e % D, rg = rb * MP + r;
       if (rg >= p.M) continue;
       const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;

@@ -27,7 +27,7 @@ __host__ __device__ constexpr size_t round_up_sz(size_t a, size_t b) { return (a
 // tiles of `mp` (a power of two); a unit of work is one (sequence, kv head, row
 // tile), and `tt` is the number of tokens staged per pipeline stage.
 struct Variant {
-  int path;         // 0: CUDA-core kernel (rows <= 8), 1: tensor-core kernel
+  int path;         // 0: CUDA-core kernel, 1: mma.sync kernel, 2: tcgen05 kernel
   int rows;         // M = G * Sq
   int mp;           // rows per unit (padded to a power of two)
   int rb;           // row tiles per kv head
@@ -74,17 +74,28 @@ inline int decode_merge_limit(int split_merge, int mp, int head_dim) {
   return n > 2 ? n : 2;
 }
 
+// Query rows per kv head above which a 128-dim head runs on the tcgen05 kernel.
+constexpr int kTcMinRows = 33;
+
 // Everything but the grid size, which needs the device (see api.cu).
-// Every cache whose tile row is at least one 128-byte slab runs on tensor cores, with the
-// query rows of a kv head padded to 16, 32 or 64 (larger groups are cut into 64-row tiles):
-// even a tile of one real row in sixteen costs less there than the CUDA-core arithmetic.
-// A 64-dim fp8 cache (64-byte rows) runs on the CUDA-core kernel, in tiles of up to 8 rows.
+// Every cache whose tile row is at least one 128-byte slab runs on tensor cores: a 16-bit
+// cache with head dim 128 and more than 32 query rows per kv head on tcgen05 (row tiles of
+// 64 or 128, the MMA always 128 rows), otherwise on mma.sync with the rows padded to 16, 32
+// or 64 (larger groups cut into 64-row tiles): even a tile of one real row in sixteen costs
+// less there than CUDA-core arithmetic.  (fp8 caches stay on mma.sync, which widens them in
+// registers: the tcgen05 kernel has to widen them in shared memory first, and measured
+// slower.)  A 64-dim fp8 cache (64-byte rows) runs on the CUDA-core kernel, in tiles of up
+// to 8 rows.
 inline Variant make_variant(const pa_config& c) {
   Variant v{};
   v.rows = (c.num_q_heads / c.num_kv_heads) * c.max_q_len;
   v.bpe = c.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
   v.path = c.head_dim * v.bpe >= 128 ? 1 : 0;
-  if (v.path == 1)
+  if (v.path == 1 && c.head_dim == 128 && v.rows >= kTcMinRows && c.kv_dtype != PA_FP8_E4M3)
+    v.path = 2;
+  if (v.path == 2)
+    v.mp = v.rows <= 64 ? 64 : 128;
+  else if (v.path == 1)
     v.mp = v.rows >= kMmaMaxRows ? kMmaMaxRows : (v.rows <= 16 ? 16 : pow2_at_least(v.rows));
   else
     v.mp = v.rows <= kSimtMaxRows ? pow2_at_least(v.rows) : kSimtMaxRows;
@@ -94,8 +105,9 @@ inline Variant make_variant(const pa_config& c) {
   v.units = c.batch * c.num_kv_heads * v.rb;
   const int kvk = c.kv_dtype == PA_FP8_E4M3 ? 2 : (c.kv_dtype == PA_FP16 ? 1 : 0);
   const bool toks = c.kv_scale_mode == PA_SCALE_PER_TOKEN;
-  v.ctas_per_sm = v.path == 1 ? mma_ctas_per_sm(c.head_dim, v.mp, kvk, toks)
-                              : simt_ctas_per_sm(c.head_dim, v.mp, kvk, toks);
+  v.ctas_per_sm = v.path == 2   ? 1
+                  : v.path == 1 ? mma_ctas_per_sm(c.head_dim, v.mp, kvk, toks)
+                                : simt_ctas_per_sm(c.head_dim, v.mp, kvk, toks);
   v.ns_dec = decode_merge_limit(c.split_merge, v.mp, c.head_dim);
   v.ctas = 0;
   return v;

@@ -67,6 +67,7 @@ def _pow2_at_least(x):
 SIMT_MAX_ROWS = 8
 TILE_BYTES = 16384
 ITEM_COST_TILES = 3
+TC_MIN_ROWS = 33
 DECODE_MERGE_FLOATS = 32768
 
 
@@ -82,7 +83,9 @@ def decode_merge_limit(split_merge: int, mp: int, head_dim: int) -> int:
 def variant(cfg: pa.PaConfig, ctas: int):
     rows = (cfg.num_q_heads // cfg.num_kv_heads) * cfg.max_q_len
     bpe = 1 if cfg.kv_dtype == pa.FP8_E4M3 else 2
-    if cfg.head_dim * bpe >= 128:  # tensor-core kernel
+    if bpe == 2 and cfg.head_dim == 128 and rows >= TC_MIN_ROWS:  # tcgen05
+        mp = 64 if rows <= 64 else 128
+    elif cfg.head_dim * bpe >= 128:  # mma.sync kernel
         mp = 64 if rows >= 64 else (16 if rows <= 16 else _pow2_at_least(rows))
     else:
         mp = _pow2_at_least(rows) if rows <= SIMT_MAX_ROWS else SIMT_MAX_ROWS
