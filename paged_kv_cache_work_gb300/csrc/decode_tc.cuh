@@ -15,8 +15,11 @@
 //               decode_common.cuh);
 //   warps 6-7   (fp8 caches) widen each step's 64 rows of K and V to f16 in shared memory,
 //               two steps ahead, and release the ring stage once its rows are widened.
-// The unit's query rows sit in shared memory (128 rows, 128-byte swizzled, K-major; for fp8
-// caches as f16, which holds every e4m3 value exactly).
+// The unit's query rows (Q, as 16-bit pairs: lane = row), the logits S (two buffers), the
+// probabilities P (two buffers) and the output accumulator O all live in tensor memory, so
+// shared memory carries only K and V.  The instances built are the 16-bit caches; the fp8
+// roles are kept but not dispatched, because widening fp8 in shared memory measured slower
+// than the mma.sync kernel's widening in registers.
 #pragma once
 
 #include "decode_common.cuh"
