@@ -26,9 +26,9 @@
 
 namespace pa {
 
-template <int MP_, int KVK_, bool TOKS_>
+template <int D_, int MP_, int KVK_, bool TOKS_>
 struct TcTraits {
-  static constexpr int D = 128;
+  static constexpr int D = D_;  // 128 or 256
   static constexpr int MP = MP_;  // query rows of a unit; the MMA always has M = 128
   static constexpr int KVK = KVK_;
   static constexpr bool TOKS = TOKS_;
@@ -39,7 +39,7 @@ struct TcTraits {
   static constexpr int NW = 6 + NCW;
   static constexpr int NTHREADS = NW * 32;
   static constexpr int TT = kTileBytes / (D * BPE);  // tokens per stage: 64, or 128 for fp8
-  static constexpr int SUB = 64;                     // tokens per MMA step
+  static constexpr int SUB = FP8 ? 64 : TT;          // tokens per MMA step: 64, or 32 for D 256
   static constexpr int NSUB = TT / SUB;
   static constexpr int NSTAGE = FP8 ? 3 : 6;
   static constexpr int NQ = 1;
@@ -65,11 +65,18 @@ struct TcTraits {
   static constexpr int NBAR = 2 * NSTAGE + NQ + 18;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 16 + 1024;
   static constexpr int CTAS_PER_SM = 1;
-  // Tensor memory (lane = query row, 32-bit columns): S buffers [0, 64) and [64, 128) fp32,
-  // O [128, 256) fp32, Q [256, 320) and P buffers [320, 352), [352, 384) as 16-bit pairs.
+  // Tensor memory (lane = query row, 32-bit columns): two S buffers of SUB fp32 columns, O
+  // (D fp32 columns), Q (D / 2 columns of 16-bit pairs) and two P buffers (SUB / 2 columns).
+  // Head dim 128: S [0, 128), O [128, 256), Q [256, 320), P [320, 384).  Head dim 256
+  // (32-token steps): S [0, 64), Q [64, 192), P [192, 224), O [256, 512).
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = 128, COL_Q = 256, COL_P = 320;
+  static constexpr uint32_t COL_O = D == 256 ? 256 : 2 * SUB;
+  static constexpr uint32_t COL_Q = D == 256 ? 2 * SUB : COL_O + D;
+  static constexpr uint32_t COL_P = COL_Q + D / 2;
+  static_assert(COL_P + SUB <= TMEM_COLS && (D != 256 || COL_P + SUB <= COL_O), "tensor memory");
   static_assert(MP == 64 || MP == 128, "row tile");
+  static_assert(D == 128 || D == 256, "head dim");
+  static_assert(SUB == 32 || SUB == 64, "step");
   static_assert(TT % SUB == 0, "tile");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -114,6 +121,24 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[3
       "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
       "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+// A row of P (N packed 16-bit pairs) into tensor memory.
+template <int N>
+__device__ __forceinline__ void tmem_st_p(uint32_t taddr, const uint32_t (&v)[N]) {
+  if constexpr (N == 32)
+    tmem_st32u(taddr, v);
+  else
+    tmem_st16u(taddr, v);
 }
 
 // Arrive on `bar` once every MMA this thread issued so far has completed.
@@ -195,14 +220,14 @@ struct TcStep {
   int tok0, c0, n;
   bool last;
 };
-__device__ __forceinline__ TcStep tc_step(int t0, int t1, int j, int tt, int nsub) {
+__device__ __forceinline__ TcStep tc_step(int t0, int t1, int j, int tt, int nsub, int sub) {
   TcStep q;
   const int k = j / nsub;
-  q.c0 = (j % nsub) * 64;
+  q.c0 = (j % nsub) * sub;
   q.tok0 = t0 + k * tt;
   const int n_in = min(tt, t1 - q.tok0);
-  q.n = min(64, n_in - q.c0);
-  q.last = q.c0 + 64 >= n_in;
+  q.n = min(sub, n_in - q.c0);
+  q.last = q.c0 + sub >= n_in;
   return q;
 }
 
@@ -233,11 +258,12 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-template <int MP, int KVK, int QK, bool TOKS>
-__global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
+template <int D_, int MP, int KVK, int QK, bool TOKS>
+__global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const KernelParams p) {
-  using T = TcTraits<MP, KVK, TOKS>;
+  using T = TcTraits<D_, MP, KVK, TOKS>;
+  constexpr int SUB = T::SUB;
   constexpr int D = T::D;
   constexpr bool BF = !T::FP8 && KVK == KV_BF16;  // MMA operands bf16 (else f16)
   constexpr uint32_t ID_S = umma_idesc(128, T::SUB, BF, false);
@@ -361,7 +387,7 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
         bool pv_last = false;
         int stage = 0;
         for (int j = 0; j < nsub; ++j, ++g) {
-          const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB);
+          const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB, T::SUB);
           if (q.c0 == 0) {
             stage = tile_ctr % T::NSTAGE;
             if constexpr (!T::FP8) wait_bar(&full[stage], (tile_ctr / T::NSTAGE) & 1);
@@ -446,7 +472,7 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
         const uint4* qrow = reinterpret_cast<const uint4*>(
             reinterpret_cast<const char*>(p.q) + ((((size_t)b * p.Sq + qi) * p.Hq + hq) * D) * 2);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < D / 64; ++h) {
           uint32_t w[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -475,7 +501,7 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
 
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nsub; ++j, ++g) {
-        const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB);
+        const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB, T::SUB);
         if (in_dec && j + 1 == nsub && stid == 0) cnt_seen = ld_acquire_gpu(&p.unit_cnt[u]);
         if (!T::FP8 && q.n < T::SUB) {
           // the zeroing below writes into the ring stage: the tile must have landed (the
@@ -486,8 +512,11 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
         wait_bar(&s_full[g & 1], sfull_ph[g & 1]);
         sfull_ph[g & 1] ^= 1u;
         tc_fence_after();
-        float x[64];
-        tmem_ld64(t_s + (g & 1) * T::SUB + lane_off, x);
+        float x[SUB];
+        if constexpr (SUB == 64)
+          tmem_ld64(t_s + (g & 1) * SUB + lane_off, x);
+        else
+          tmem_ld32(t_s + (g & 1) * SUB + lane_off, x);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[g & 1]);
@@ -502,7 +531,7 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
         // ---- online softmax of this thread's row (log2 units), two logits per instruction
         const float2 s2 = make_float2(qk_scale, qk_scale), z2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < SUB / 2; ++i) {
           float2 y = ffma2(make_float2(x[2 * i], x[2 * i + 1]), s2, z2);
           if constexpr (TOKS) y = ffma2(y, make_float2(ksc[2 * i], ksc[2 * i + 1]), z2);
           x[2 * i] = y.x;
@@ -512,12 +541,12 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
         // most steps have none
         if (q.n < T::SUB || q.tok0 + q.c0 + T::SUB > lim) {
 #pragma unroll
-          for (int jj = 0; jj < 64; ++jj)
+          for (int jj = 0; jj < SUB; ++jj)
             if (jj >= q.n || q.tok0 + q.c0 + jj >= lim) x[jj] = -INFINITY;
         }
         float mx = -INFINITY;
 #pragma unroll
-        for (int jj = 0; jj < 64; jj += 2) mx = fmaxf(mx, fmaxf(x[jj], x[jj + 1]));
+        for (int jj = 0; jj < SUB; jj += 2) mx = fmaxf(mx, fmaxf(x[jj], x[jj + 1]));
         const bool need = mx > m_run + 8.f;  // lazy rescale: only when the max grows by 2^8
         const bool rescale = __any_sync(kFull, need);
         const float mn = need ? mx : m_run;
@@ -526,15 +555,15 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
         // this thread's row of P, packed: 64 tokens = eight 16-byte chunks; a masked logit
         // (-inf) gives exp2 = 0, and a row with no visible key so far has only zeros
         float lsum = 0.f;
-        uint32_t pk[32];
+        uint32_t pk[SUB / 2];
         if (m_run == -INFINITY) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = 0u;
+          for (int i = 0; i < SUB / 2; ++i) pk[i] = 0u;
         } else {
           const float2 nm = make_float2(-m_run, -m_run), one2 = make_float2(1.f, 1.f);
           float2 ls2 = z2;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < SUB / 2; ++i) {
             const float2 t = ffma2(make_float2(x[2 * i], x[2 * i + 1]), one2, nm);
             float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
             ls2 = ffma2(make_float2(p0, p1), one2, ls2);
@@ -562,7 +591,7 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
           tmem_wait_st();
         }
         if (g >= 2) wait_pv_step(g - 2);  // P buffer g % 2 was last read by the PV of step g - 2
-        tmem_st32u(t_p + (g & 1) * (T::SUB / 2) + lane_off, pk);
+        tmem_st_p<SUB / 2>(t_p + (g & 1) * (SUB / 2) + lane_off, pk);
         tmem_wait_st();
         if constexpr (!T::FP8) {
           if (q.n < T::SUB) {
@@ -603,10 +632,10 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
       }
       const bool to_out = slot < 0 || fin;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < D / 64; ++h) {
         float o[64];
         tmem_ld64(t_o + lane_off + 64 * h, o);
-        if (h == 1) {
+        if (h == D / 64 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(o_free);  // the next item's first PV may overwrite O
@@ -684,7 +713,7 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
         if (t1 <= t0) continue;
         const int nsub = ceil_div(t1 - t0, T::SUB);
         for (int j = 0; j < nsub; ++j, ++g) {
-          const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB);
+          const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB, T::SUB);
           if (q.c0 == 0) {
             stage = tile_ctr % T::NSTAGE;
             wait_bar(&full[stage], (tile_ctr / T::NSTAGE) & 1);
@@ -745,11 +774,11 @@ __global__ void __launch_bounds__(TcTraits<MP, KVK, TOKS>::NTHREADS, 1)
   grid_dependents_launch();
 }
 
-template <int MP, int KVK, int QK, bool TOKS>
+template <int D, int MP, int KVK, int QK, bool TOKS>
 cudaError_t launch_tc_instance(const KernelParams& prm, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, int grid, cudaStream_t s) {
-  using T = TcTraits<MP, KVK, TOKS>;
-  auto kern = decode_tc_kernel<MP, KVK, QK, TOKS>;
+  using T = TcTraits<D, MP, KVK, TOKS>;
+  auto kern = decode_tc_kernel<D, MP, KVK, QK, TOKS>;
   static bool attr_set = false;  // benign race: every caller sets the same value
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);

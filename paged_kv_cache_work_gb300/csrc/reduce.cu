@@ -23,6 +23,8 @@ int simt_ctas_per_sm_d256(int, int, bool);
 
 cudaError_t launch_tc_d128(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                            int, int, bool, cudaStream_t);
+cudaError_t launch_tc_d256(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
+                           int, int, bool, cudaStream_t);
 
 int mma_ctas_per_sm_d64(int, int, bool);
 int mma_ctas_per_sm_d128(int, int, bool);
@@ -94,8 +96,11 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CU
   const KernelParams prm = make_kernel_params(a);
   const bool toks = a.scale_mode == PA_SCALE_PER_TOKEN;
   if (a.v.path == 2) {
-    if (a.p.head_dim != 128) return cudaErrorNotSupported;
-    return launch_tc_d128(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+    switch (a.p.head_dim) {
+      case 128: return launch_tc_d128(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+      case 256: return launch_tc_d256(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+      default: return cudaErrorNotSupported;
+    }
   }
   if (a.v.path == 1) {
     switch (a.p.head_dim) {

@@ -83,7 +83,7 @@ def decode_merge_limit(split_merge: int, mp: int, head_dim: int) -> int:
 def variant(cfg: pa.PaConfig, ctas: int):
     rows = (cfg.num_q_heads // cfg.num_kv_heads) * cfg.max_q_len
     bpe = 1 if cfg.kv_dtype == pa.FP8_E4M3 else 2
-    if bpe == 2 and cfg.head_dim == 128 and rows >= TC_MIN_ROWS:  # tcgen05
+    if bpe == 2 and cfg.head_dim >= 128 and rows >= TC_MIN_ROWS:  # tcgen05
         mp = 64 if rows <= 64 else 128
     elif cfg.head_dim * bpe >= 128:  # mma.sync kernel
         mp = 64 if rows >= 64 else (16 if rows <= 16 else _pow2_at_least(rows))

@@ -128,7 +128,7 @@ EDGE = [
     # mma.sync kernel: row tiles of 16, 32 and 64
     ("mma_rows12_padded", dict(batch=3, max_q_len=1, num_q_heads=24, num_kv_heads=2,
                                head_dim=128, block_size=16, ctx=[77, 300, 16])),
-    ("mma_d256_rows100_two_tiles", dict(batch=2, max_q_len=4, num_q_heads=25, num_kv_heads=1,
+    ("d256_rows100", dict(batch=2, max_q_len=4, num_q_heads=25, num_kv_heads=1,
                                         head_dim=256, block_size=64, ctx=[200, 517],
                                         causal=True)),
     ("mma_fp16_rows32", dict(batch=2, max_q_len=2, num_q_heads=16, num_kv_heads=1, head_dim=128,
@@ -162,8 +162,8 @@ def test_edge_cases(name, kw, cuda_device, pa):
     assert pa.read_flags(ws) == 0
 
 
-# The tcgen05 kernel: head dim 128 with more than 32 query rows per kv head (tiles of 64 or
-# 128 rows, MMA always 128 rows), bf16/fp16 operands, fp8 widened to f16 in shared memory.
+# The tcgen05 kernel: 16-bit caches, head dim 128 or 256, more than 32 query rows per kv head
+# (tiles of 64 or 128 rows, MMA always 128 rows).  The fp8 cases here run on mma.sync.
 TC = [
     ("rows33_padded_causal", dict(batch=3, max_q_len=3, num_q_heads=11, num_kv_heads=1,
                                   block_size=16, ctx=[70, 300, 129], causal=True)),
@@ -189,6 +189,13 @@ TC = [
                               causal=True)),
     ("not_causal_tiny", dict(batch=2, max_q_len=2, num_q_heads=24, num_kv_heads=1,
                              block_size=16, ctx=[1, 3])),
+    ("d256_rows64_causal", dict(head_dim=256, batch=3, max_q_len=64, num_q_heads=2,
+                                num_kv_heads=2, block_size=32, ctx=[64, 300, 1029], causal=True)),
+    ("d256_fp16_rows100_bs16", dict(head_dim=256, batch=2, max_q_len=4, num_q_heads=25,
+                                    num_kv_heads=1, block_size=16, ctx=[200, 77], q_dtype="fp16",
+                                    kv_dtype="fp16", causal=True)),
+    ("d256_rows256_two_tiles", dict(head_dim=256, batch=2, max_q_len=16, num_q_heads=16,
+                                    num_kv_heads=1, block_size=64, ctx=[300, 40], causal=True)),
 ]
 
 
@@ -196,7 +203,7 @@ TC = [
 @pytest.mark.parametrize("name,kw", TC, ids=[c[0] for c in TC])
 def test_tcgen05_kernel(name, kw, ctas, cuda_device, pa):
     rng = np.random.default_rng(zlib.crc32(name.encode()) + ctas)
-    inp, _ = random_problem(rng, head_dim=128, **kw)
+    inp, _ = random_problem(rng, **{"head_dim": 128, **kw})
     ref_out, ref_lse = oracle.decode(inp, "f32")
     out, lse, ws, _ = run(W.to_device(inp, cuda_device), num_ctas=ctas)
     compare(out, lse, ref_out, ref_lse, kw.get("kv_dtype", "bf16"))
