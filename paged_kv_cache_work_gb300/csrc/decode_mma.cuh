@@ -173,6 +173,9 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   }
   __syncthreads();
   grid_dependency_wait();  // the work list comes from the planner launched just before
+  // the next kernel may start launching now: it is held in its own grid_dependency_wait
+  // until this grid has completed, and it cannot take the place of a CTA of this grid
+  grid_dependents_launch();
 
   const int it_begin = p.item_off[blockIdx.x], it_end = p.item_off[blockIdx.x + 1];
   TileProducer<T> prod;
@@ -590,7 +593,6 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   named_barrier_sync(1, T::NTHREADS);  // no copy in flight: stage 0 is free for the merge
   finish_pending<D, MP, QK, T::NW>(p, pend, reinterpret_cast<float*>(smem), T::STAGE / 4, mlbuf);
   zero_empty_units<D, MP, QK, T::NTHREADS>(p);
-  grid_dependents_launch();
 }
 
 template <int D, int MP, int KVK, int QK, bool TOKS>

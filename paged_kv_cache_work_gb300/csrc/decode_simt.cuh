@@ -259,6 +259,9 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   }
   __syncthreads();
   grid_dependency_wait();  // the work list comes from the planner launched just before
+  // the next kernel may start launching now: it is held in its own grid_dependency_wait
+  // until this grid has completed, and it cannot take the place of a CTA of this grid
+  grid_dependents_launch();
 
   const int it_begin = p.item_off[blockIdx.x], it_end = p.item_off[blockIdx.x + 1];
   TileProducer<T> prod;
@@ -471,7 +474,6 @@ __global__ void __launch_bounds__(SimtTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
       p, pend, reinterpret_cast<float*>(smem + (T::OWN_MERGE ? T::OFF_MERGE_O : 0)),
       T::MERGE_O / 4, mbuf);
   zero_empty_units<D, MP, QK, T::NTHREADS>(p);
-  grid_dependents_launch();
 }
 
 template <int D, int MP, int KVK, int QK, bool TOKS>

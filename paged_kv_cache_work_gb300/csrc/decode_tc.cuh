@@ -334,6 +334,9 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   const uint32_t tmem = *tslot;
   const uint32_t t_s = tmem, t_o = tmem + T::COL_O, t_q = tmem + T::COL_Q, t_p = tmem + T::COL_P;
   grid_dependency_wait();  // the work list comes from the planner launched just before
+  // the next kernel may start launching now: it is held in its own grid_dependency_wait
+  // until this grid has completed, and it cannot take the place of a CTA of this grid
+  grid_dependents_launch();
 
   const int it_begin = p.item_off[blockIdx.x], it_end = p.item_off[blockIdx.x + 1];
   auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
@@ -771,7 +774,6 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(T::TMEM_COLS));
   }
-  grid_dependents_launch();
 }
 
 template <int D, int MP, int KVK, int QK, bool TOKS>

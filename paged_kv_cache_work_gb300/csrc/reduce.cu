@@ -145,6 +145,9 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
   __shared__ float s_m[kReduceWarps], s_w[kReduceWarps];
   __shared__ float4 s_acc[kReduceWarps][D4];
   grid_dependency_wait();  // partials come from the decode kernel launched just before
+  // the next kernel may start launching now: it is held in its own grid_dependency_wait
+  // until this grid has completed, and it cannot take the place of a CTA of this grid
+  grid_dependents_launch();
   const int nred = p.hdr[HDR_NRED];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int w = blockIdx.x; w < nred * p.MP; w += gridDim.x) {
@@ -246,7 +249,6 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
     if (c == 0 && p.lse) p.lse[row] = Wt > 0.f ? (mt + fast_log2(Wt)) * kLn2 : -INFINITY;
     __syncthreads();  // shared results are rewritten by the next row
   }
-  grid_dependents_launch();
 }
 
 template <int D>
