@@ -62,16 +62,18 @@ int mma_ctas_per_sm(int head_dim, int mp, int kvk, bool toks);
 // Largest row tile of the tensor-core decode kernel.
 constexpr int kMmaMaxRows = 64;
 
-// Partials the last CTA of a unit reads in the decode's own merge: one SM pulls them from
-// L2 while the rest of the grid may be idle, so larger merges go to the reduce kernel.
-constexpr int kDecodeMergeFloats = 32768;
+// Pieces of a split unit the decode kernel merges itself under PA_MERGE_AUTO.  The merge
+// runs on one SM after the CTA's other work while most of the grid may already be idle; a
+// unit of two pieces costs one extra partial there, but beyond that the reduce kernel, which
+// spreads every unit's rows over the whole GPU, finishes sooner (measured on 128-dim caches:
+// five-piece units of 16-row tiles took 10 us longer per step merged in the decode).
+constexpr int kDecodeMergePieces = 2;
 
 // The most pieces of a split unit the decode kernel merges itself (1: none).
-inline int decode_merge_limit(int split_merge, int mp, int head_dim) {
+inline int decode_merge_limit(int split_merge) {
   if (split_merge == PA_MERGE_IN_DECODE) return 1 << 30;
   if (split_merge == PA_MERGE_IN_REDUCE) return 1;
-  const int n = kDecodeMergeFloats / (mp * head_dim);
-  return n > 2 ? n : 2;
+  return kDecodeMergePieces;
 }
 
 // Query rows per kv head above which a 128-dim head runs on the tcgen05 kernel.
@@ -108,7 +110,7 @@ inline Variant make_variant(const pa_config& c) {
   v.ctas_per_sm = v.path == 2   ? 1
                   : v.path == 1 ? mma_ctas_per_sm(c.head_dim, v.mp, kvk, toks)
                                 : simt_ctas_per_sm(c.head_dim, v.mp, kvk, toks);
-  v.ns_dec = decode_merge_limit(c.split_merge, v.mp, c.head_dim);
+  v.ns_dec = decode_merge_limit(c.split_merge);
   v.ctas = 0;
   return v;
 }

@@ -68,16 +68,16 @@ SIMT_MAX_ROWS = 8
 TILE_BYTES = 16384
 ITEM_COST_TILES = 3
 TC_MIN_ROWS = 33
-DECODE_MERGE_FLOATS = 32768
+DECODE_MERGE_PIECES = 2
 
 
-def decode_merge_limit(split_merge: int, mp: int, head_dim: int) -> int:
+def decode_merge_limit(split_merge: int) -> int:
     """Most pieces of a split unit that the decode kernel merges itself (pa_split_merge)."""
     if split_merge == pa.MERGE_IN_DECODE:
         return 1 << 30
     if split_merge == pa.MERGE_IN_REDUCE:
         return 1
-    return max(2, DECODE_MERGE_FLOATS // (mp * head_dim))
+    return DECODE_MERGE_PIECES
 
 
 def variant(cfg: pa.PaConfig, ctas: int):
@@ -92,7 +92,7 @@ def variant(cfg: pa.PaConfig, ctas: int):
     rb = -(-rows // mp)
     tt = TILE_BYTES // (cfg.head_dim * bpe)
     return dict(rows=rows, mp=mp, rb=rb, tt=tt, units=cfg.batch * cfg.num_kv_heads * rb,
-                ctas=ctas, ns_dec=decode_merge_limit(cfg.split_merge, mp, cfg.head_dim),
+                ctas=ctas, ns_dec=decode_merge_limit(cfg.split_merge),
                 item_cost=ITEM_COST_TILES * tt)
 
 
