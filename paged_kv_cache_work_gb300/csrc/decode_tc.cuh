@@ -1,25 +1,30 @@
 // Fifth-generation tensor-core decode (tcgen05, accumulators in tensor memory) for large
-// query tiles: 33 to 128 query rows per kv head, head dim 128.
+// query tiles: 33 to 128 query rows per kv head, head dim 128 or 256, 16-bit caches.
 //
-// The CTA is split into roles that talk only through mbarriers, so copies, conversions,
-// MMAs and the softmax of different 64-token steps overlap:
-//   warp 0      streams the items' K/V tiles through the TMA ring (TileProducer);
-//   warp 1      one thread issues, per step g, S = Q K^T (M = 128, N = 64, K = 128) into
-//               tensor-memory buffer g % 2, and then O += P V for step g - 1 (M = 128,
-//               N = 128, K = 64, V read as an MN-major operand), so the next logits are being
-//               computed while the softmax works on the current ones;
-//   warps 2-5   one query row per thread: load the row's 64 logits with tcgen05.ld, online
-//               softmax in registers (a row never leaves its thread), write the row of P into
-//               a 128-byte-swizzled shared tile; at the end of an item load O from tensor
-//               memory and write the output or the split partial (merge protocol of
-//               decode_common.cuh);
-//   warps 6-7   (fp8 caches) widen each step's 64 rows of K and V to f16 in shared memory,
-//               two steps ahead, and release the ring stage once its rows are widened.
-// The unit's query rows (Q, as 16-bit pairs: lane = row), the logits S (two buffers), the
-// probabilities P (two buffers) and the output accumulator O all live in tensor memory, so
-// shared memory carries only K and V.  The instances built are the 16-bit caches; the fp8
-// roles are kept but not dispatched, because widening fp8 in shared memory measured slower
-// than the mma.sync kernel's widening in registers.
+// A step is a tile of 64 tokens.  The CTA is split into roles that talk only through
+// mbarriers, so copies, MMAs and the softmax of different steps overlap:
+//   warp 0      streams the items' K and V tiles through two TMA rings (TcProducer) of
+//               96 KB each: a K slot is released by the S that read it and a V slot by its
+//               PV, and K is copied one step ahead of V;
+//   warp 1      one thread issues, per step g, S = Q K^T (M = 128, N = 64, K = head dim)
+//               into tensor-memory buffer g % NSP, and then O += P V for step
+//               g - (NSP - 1) (M = 128, N = head dim, K = 64, V read as an MN-major
+//               operand), so the in-order tensor pipe holds the next logits ahead of any
+//               PV that waits for the softmax;
+//   warps 2-5   one query row per thread: load the row's logits with tcgen05.ld, online
+//               softmax in registers (a row never leaves its thread), write the row of P as
+//               16-bit pairs over the first half of the same logits buffer; at the end of an
+//               item load O from tensor memory and write the output or the split partial
+//               (merge protocol of decode_common.cuh).
+// Buffer g % NSP holds S(g) and then P(g) until the PV of step g has read it, so the MMA
+// thread waits for that PV before it writes S(g + NSP) there: NSP = 4 at head dim 128 and
+// 2 at head dim 256, as many as tensor memory holds next to O and the query rows (Q, as
+// 16-bit pairs: lane = row).  Shared memory carries only K and V.
+//
+// A tcgen05.mma of K = 16 occupies the tensor pipe about equally long at every N up to
+// 256, so these N = 64 logits use a quarter of its peak: at head dim 256 (16 S MMAs and 4
+// PV MMAs per 64 KB of cache) the pipe keeps up with HBM, at head dim 128 it is close to
+// being the limit.
 #pragma once
 
 #include "decode_common.cuh"
@@ -28,56 +33,48 @@ namespace pa {
 
 template <int D_, int MP_, int KVK_, bool TOKS_>
 struct TcTraits {
-  static constexpr int D = D_;  // 128 or 256
+  static constexpr int D = D_;    // 128 or 256
   static constexpr int MP = MP_;  // query rows of a unit; the MMA always has M = 128
   static constexpr int KVK = KVK_;
   static constexpr bool TOKS = TOKS_;
   static constexpr bool FP8 = KVK == KV_FP8;
-  static constexpr int BPE = FP8 ? 1 : 2;
-  static constexpr int W_PROD = 0, W_MMA = 1, W_SOFT = 2, W_CONV = 6;
-  static constexpr int NCW = FP8 ? 2 : 0;  // converter warps
-  static constexpr int NW = 6 + NCW;
+  static constexpr int BPE = 2;
+  static constexpr int W_PROD = 0, W_MMA = 1, W_SOFT = 2;
+  static constexpr int NW = 6;
   static constexpr int NTHREADS = NW * 32;
-  static constexpr int TT = kTileBytes / (D * BPE);  // tokens per stage: 64, or 128 for fp8
-  static constexpr int SUB = FP8 ? 64 : TT;          // tokens per MMA step: 64, or 32 for D 256
-  static constexpr int NSUB = TT / SUB;
-  static constexpr int NSTAGE = FP8 ? 3 : 6;
-  static constexpr int NQ = 1;
-  static constexpr int QSLOT = 0;
-  static constexpr bool WITH_Q = false;
+  static constexpr int TT = kTcStepTokens;  // tokens per tile and per MMA step: 64
+  static constexpr int SUB = TT;
+  static constexpr int KTILE = TT * D * BPE;         // 16 KB, or 32 KB at head dim 256
+  static constexpr int NSTAGE = 98304 / KTILE;       // slots of each ring: 6, or 3 (96 KB)
   static constexpr int ROWB = 128;             // swizzled slabs of 128 bytes per row
   static constexpr int NSLAB = D * BPE / 128;  // slabs of a cache tile row
-  static constexpr int KTILE = TT * D * BPE;
-  static constexpr int STAGE = round_up(2 * KTILE + (TOKS ? 2 * TT * 4 : 0), 1024);
-  static constexpr int OFF_Q = 0;                       // (query rows live in tensor memory)
-  static constexpr int OFF_CV = NSTAGE * STAGE;         // fp8: 64 tokens of K, then V, as f16
-  static constexpr int CV_SLAB = SUB * 128;             // one 64-dim slab of 64 converted rows
-  static constexpr int CV_BUF = 2 * 2 * CV_SLAB;        // K and V of one step
-  static constexpr int CV_BYTES = FP8 ? 2 * CV_BUF : 0;  // two steps
-  static constexpr int KSLAB = FP8 ? CV_SLAB : TT * 128;  // slab stride of the K and V operands
-  static constexpr int OFF_SC = OFF_CV + CV_BYTES;        // per-token scales of two steps
-  static constexpr int SC_BYTES = TOKS ? 2 * 2 * SUB * 4 : 0;
-  static constexpr int OFF_ML = OFF_SC + SC_BYTES;
+  // S/P buffers in tensor memory: four at head dim 128 (S(g) waits only for the PV of
+  // step g - 4), two at 256
+  static constexpr int NSP = D == 128 ? 4 : 2;
+  static constexpr int OFF_K = 0;                       // K ring: NSTAGE tiles
+  static constexpr int OFF_V = OFF_K + NSTAGE * KTILE;  // V ring: NSTAGE tiles
+  static constexpr int STAGE = 2 * KTILE;               // (scratch capacity at the end)
+  static constexpr int KSLAB = TT * 128;                // slab stride of the K and V operands
+  static constexpr int OFF_ML = OFF_V + NSTAGE * KTILE;
   static constexpr int ML_BYTES = round_up(2 * MP * 4, 128);
   static constexpr int OFF_BAR = round_up(OFF_ML + ML_BYTES, 64);
-  // full, empty, (unused query slot), s_full x2, s_free x2, p_full x2, pv_done x2, o_free,
-  // q_full, cv_full x2, cv_free x2, mma_end, sc_full x2
-  static constexpr int NBAR = 2 * NSTAGE + NQ + 18;
+  // full_k, empty_k, full_v, empty_v (NSTAGE each), s_full, p_full, pv_done (NSP each),
+  // o_free, q_full, mma_end
+  static constexpr int NBAR = 4 * NSTAGE + 3 * NSP + 3;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 16 + 1024;
   static constexpr int CTAS_PER_SM = 1;
-  // Tensor memory (lane = query row, 32-bit columns): two S buffers of SUB fp32 columns, O
-  // (D fp32 columns), Q (D / 2 columns of 16-bit pairs) and two P buffers (SUB / 2 columns).
-  // Head dim 128: S [0, 128), O [128, 256), Q [256, 320), P [320, 384).  Head dim 256
-  // (32-token steps): S [0, 64), Q [64, 192), P [192, 224), O [256, 512).
+  // Tensor memory (lane = query row, 32-bit columns): NSP S/P buffers of SUB fp32 columns
+  // (P, SUB / 2 columns of 16-bit pairs, overwrites the first half of its own S), O (D fp32
+  // columns) and Q (D / 2 columns of 16-bit pairs).  Head dim 128: S/P [0, 256), O
+  // [256, 384), Q [384, 448).  Head dim 256: S/P [0, 128), Q [128, 256), O [256, 512).
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = D == 256 ? 256 : 2 * SUB;
-  static constexpr uint32_t COL_Q = D == 256 ? 2 * SUB : COL_O + D;
-  static constexpr uint32_t COL_P = COL_Q + D / 2;
-  static_assert(COL_P + SUB <= TMEM_COLS && (D != 256 || COL_P + SUB <= COL_O), "tensor memory");
+  static constexpr uint32_t COL_O = D == 256 ? 256 : NSP * SUB;
+  static constexpr uint32_t COL_Q = D == 256 ? NSP * SUB : COL_O + D;
+  static_assert(NSP * SUB + D + D / 2 <= (int)TMEM_COLS, "tensor memory");
+  static_assert(!FP8 && !TOKS, "16-bit caches only");
   static_assert(MP == 64 || MP == 128, "row tile");
   static_assert(D == 128 || D == 256, "head dim");
-  static_assert(SUB == 32 || SUB == 64, "step");
-  static_assert(TT % SUB == 0, "tile");
+  static_assert(SUB == 64, "step");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -209,28 +206,6 @@ __device__ __forceinline__ uint32_t pack16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
   }
 }
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t w) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
-
-// One 64-token step g of an item: first token of its tile, offset in the tile, tokens of the
-// item in it, and whether it is the last step of its tile.
-struct TcStep {
-  int tok0, c0, n;
-  bool last;
-};
-__device__ __forceinline__ TcStep tc_step(int t0, int t1, int j, int tt, int nsub, int sub) {
-  TcStep q;
-  const int k = j / nsub;
-  q.c0 = (j % nsub) * sub;
-  q.tok0 = t0 + k * tt;
-  const int n_in = min(tt, t1 - q.tok0);
-  q.n = min(sub, n_in - q.c0);
-  q.last = q.c0 + sub >= n_in;
-  return q;
-}
-
 // 32 lanes x 32 bits x 64 columns: thread t of warp w gets columns [col, col + 64) of lane
 // 32 (w % 4) + t, with one wait.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -258,6 +233,135 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// The TMA side of the tcgen05 kernel, run by warp 0 (all lanes, same state).  Tile n of the
+// CTA's work list goes to slot n % NSTAGE of the K ring and of the V ring; lane
+// page * NSLAB + slab copies one 128-byte column slab of one page of the tile.  The order of
+// the copies is K(0), K(1), V(0), K(2), V(1), ...: a K copy waits for the S of the tile
+// NSTAGE earlier, a V copy for its PV.
+template <class T>
+struct TcProducer {
+  struct Box {
+    int blk, row, g;
+    bool ok;
+    uint32_t nvalid;
+  };
+  const KernelParams* p;
+  const CUtensorMap* kmap;
+  const CUtensorMap* vmap;
+  char* smem;
+  uint64_t *full_k, *empty_k, *full_v, *empty_v;
+  volatile int* abort_flag;
+  int lane, it, it_end, k, ntiles, t0, t1, b, g, box_rows, nbox, blk_next;
+  uint32_t box_bytes, nk, nv;
+  bool have, next_ready;
+  int4 item_next;
+
+  __device__ __forceinline__ int block_of(int bb, int tt0, int tt1, int kk) const {
+    const int tokb = tt0 + kk * T::TT + (lane / T::NSLAB) * box_rows;
+    return (lane < nbox * T::NSLAB && tokb < tt1)
+               ? __ldg(p->bt + (size_t)bb * p->maxb + (tokb >> p->bs_shift))
+               : -1;
+  }
+
+  __device__ __forceinline__ void init(const KernelParams* prm, const CUtensorMap* km,
+                                       const CUtensorMap* vm, char* sm, uint64_t* fk,
+                                       uint64_t* ek, uint64_t* fv, uint64_t* ev,
+                                       volatile int* ab, int ln, int ib, int ie) {
+    p = prm; kmap = km; vmap = vm; smem = sm; full_k = fk; empty_k = ek; full_v = fv;
+    empty_v = ev; abort_flag = ab; lane = ln; it = ib - 1; it_end = ie; k = 0; ntiles = 0;
+    box_rows = min(p->bs, T::TT);
+    nbox = T::TT / box_rows;
+    box_bytes = (uint32_t)box_rows * T::ROWB;
+    nk = nv = 0;
+    have = next_ready = false;
+    blk_next = -1;
+    item_next = ib < ie ? p->items[ib] : make_int4(0, 0, 0, -1);
+  }
+
+  // This lane's box of the next tile of the list; false when the list is exhausted.  The
+  // block id of the tile after it is loaded here too, to land during the waits.
+  __device__ __forceinline__ bool next_tile(Box& bx) {
+    while (!have) {
+      if (++it >= it_end) return false;
+      const int4 item = item_next;
+      if (it + 1 < it_end) item_next = p->items[it + 1];
+      t0 = item.y;
+      t1 = item.z;
+      if (t1 <= t0) continue;
+      b = item.x / (p->Hkv * p->RB);
+      g = (item.x / p->RB) % p->Hkv;
+      k = 0;
+      ntiles = ceil_div(t1 - t0, T::TT);
+      if (!next_ready) blk_next = block_of(b, t0, t1, 0);
+      next_ready = false;
+      have = true;
+    }
+    const int tokb = t0 + k * T::TT + (lane / T::NSLAB) * box_rows;
+    const bool want = lane < nbox * T::NSLAB && tokb < t1;
+    bx.blk = blk_next;
+    bx.ok = want && blk_next >= 0 && blk_next < p->nblocks;
+    if (want && !bx.ok) atomicOr(p->flags, PA_FLAG_BAD_BLOCK_ID);
+    bx.nvalid = __popc(__ballot_sync(kFull, bx.ok));
+    bx.row = tokb & (p->bs - 1);
+    bx.g = g;
+    if (k + 1 < ntiles) {
+      blk_next = block_of(b, t0, t1, k + 1);
+    } else if (it + 1 < it_end && item_next.z > item_next.y) {
+      blk_next = block_of(item_next.x / (p->Hkv * p->RB), item_next.y, item_next.z, 0);
+      next_ready = true;
+    }
+    if (++k >= ntiles) have = false;
+    return true;
+  }
+
+  // Copy a tile's boxes into slot n % NSTAGE of one ring once the slot is released.
+  __device__ __forceinline__ bool issue(const Box& bx, uint32_t n, uint64_t* full,
+                                        uint64_t* empty, const CUtensorMap* map, int ring) {
+    const int s = (int)(n % T::NSTAGE);
+    if (!mbar_wait(&empty[s], ((n / T::NSTAGE) & 1) ^ 1, abort_flag)) {
+      atomicOr(p->flags, PA_FLAG_WAIT_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+    if (lane == 0) mbar_arrive_expect_tx(&full[s], bx.nvalid * box_bytes);
+    __syncwarp();
+    if (bx.ok) {
+      // slab h of page j lands at h * (TT rows) + j * (box rows), in units of ROWB bytes
+      const int page = lane / T::NSLAB, slab = lane % T::NSLAB;
+      const uint32_t dst = (uint32_t)(slab * T::TT + page * box_rows) * T::ROWB;
+      tma_load_4d(smem + ring + s * T::KTILE + dst, map, &full[s], slab * (T::ROWB / T::BPE),
+                  bx.g, bx.row, bx.blk);
+    }
+    return true;
+  }
+
+  __device__ __forceinline__ void run() {
+    Box cur, nxt;
+    if (!next_tile(cur)) return;
+    if (!issue(cur, nk, full_k, empty_k, kmap, T::OFF_K)) return;
+    ++nk;
+    while (true) {
+      const bool more = next_tile(nxt);
+      if (more) {
+        if (!issue(nxt, nk, full_k, empty_k, kmap, T::OFF_K)) return;
+        ++nk;
+      }
+      if (!issue(cur, nv, full_v, empty_v, vmap, T::OFF_V)) return;
+      ++nv;
+      if (!more) return;
+      cur = nxt;
+    }
+  }
+
+  // Let every copy this warp started land before the CTA may exit.
+  __device__ __forceinline__ void drain() {
+    for (uint32_t j = nk > (uint32_t)T::NSTAGE ? nk - T::NSTAGE : 0; j < nk; ++j)
+      mbar_wait_drain(&full_k[j % T::NSTAGE], (j / T::NSTAGE) & 1);
+    for (uint32_t j = nv > (uint32_t)T::NSTAGE ? nv - T::NSTAGE : 0; j < nv; ++j)
+      mbar_wait_drain(&full_v[j % T::NSTAGE], (j / T::NSTAGE) & 1);
+  }
+};
+
 template <int D_, int MP, int KVK, int QK, bool TOKS>
 __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -265,48 +369,38 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   using T = TcTraits<D_, MP, KVK, TOKS>;
   constexpr int SUB = T::SUB;
   constexpr int D = T::D;
-  constexpr bool BF = !T::FP8 && KVK == KV_BF16;  // MMA operands bf16 (else f16)
-  constexpr uint32_t ID_S = umma_idesc(128, T::SUB, BF, false);
+  constexpr bool BF = KVK == KV_BF16;  // MMA operands bf16 (else f16)
+  constexpr uint32_t ID_S = umma_idesc(128, SUB, BF, false);
   constexpr uint32_t ID_PV = umma_idesc(128, D, BF, true);
   constexpr int SOFT_BAR = 2;  // named barrier of the four softmax warps
   extern __shared__ char smem_raw[];
   char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
-  uint64_t* empty = full + T::NSTAGE;
-  uint64_t* qfull = empty + T::NSTAGE;
-  uint64_t* s_full = qfull + T::NQ;  // [2]
-  uint64_t* s_free = s_full + 2;     // [2]
-  uint64_t* p_full = s_free + 2;     // [2]: one per P buffer
-  uint64_t* pv_done = p_full + 2;    // [2]: the PV that read P buffer b has completed
-  uint64_t* o_free = pv_done + 2;
+  uint64_t* full_k = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
+  uint64_t* empty_k = full_k + T::NSTAGE;
+  uint64_t* full_v = empty_k + T::NSTAGE;
+  uint64_t* empty_v = full_v + T::NSTAGE;
+  uint64_t* s_full = empty_v + T::NSTAGE;  // [NSP]
+  uint64_t* p_full = s_full + T::NSP;      // [NSP]: P of the step in buffer b is written
+  uint64_t* pv_done = p_full + T::NSP;     // [NSP]: the PV that read buffer b has completed
+  uint64_t* o_free = pv_done + T::NSP;
   uint64_t* q_full = o_free + 1;
-  uint64_t* cv_full = q_full + 1;  // [2]
-  uint64_t* cv_free = cv_full + 2;  // [2]
-  uint64_t* mma_end = cv_free + 2;
-  uint64_t* sc_full = mma_end + 1;  // [2]: per-token scales of a step staged (fp8)
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sc_full + 2);
+  uint64_t* mma_end = q_full + 1;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_end + 1);
   volatile int* pend = abort_flag + 2;        // [4]: split pieces published, see finish_pending
   volatile int* cnt_seen_s = abort_flag + 6;  // published pieces of the item's unit, seen late
   uint32_t* tslot = reinterpret_cast<uint32_t*>(const_cast<int*>(abort_flag + 7));
   float* mlbuf = reinterpret_cast<float*>(smem + T::OFF_ML);
-  char* scv = smem + T::OFF_CV;
-  float* ssc = reinterpret_cast<float*>(smem + T::OFF_SC);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < T::NSTAGE; ++s) {
-      mbar_init(&full[s], TOKS ? 33 : 1);
-      mbar_init(&empty[s], T::FP8 ? T::NCW : 1);  // converter warps, or the MMA commit
+      mbar_init(&full_k[s], 1);
+      mbar_init(&empty_k[s], 1);  // the commit of the S that read the slot
+      mbar_init(&full_v[s], 1);
+      mbar_init(&empty_v[s], 1);  // the commit of the PV that read the slot
     }
-    mbar_init(&qfull[0], 32);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < T::NSP; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 4);
-      mbar_init(&cv_full[b], T::FP8 ? T::NCW : 1);
-      mbar_init(&cv_free[b], 1);
-      mbar_init(&sc_full[b], T::FP8 ? T::NCW : 1);
-    }
-    for (int b = 0; b < 2; ++b) {
       mbar_init(&p_full[b], 4);
       mbar_init(&pv_done[b], 1);
     }
@@ -332,7 +426,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t t_s = tmem, t_o = tmem + T::COL_O, t_q = tmem + T::COL_Q, t_p = tmem + T::COL_P;
+  const uint32_t t_s = tmem, t_o = tmem + T::COL_O, t_q = tmem + T::COL_Q;
   grid_dependency_wait();  // the work list comes from the planner launched just before
   // the next kernel may start launching now: it is held in its own grid_dependency_wait
   // until this grid has completed, and it cannot take the place of a CTA of this grid
@@ -348,110 +442,90 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
 
   if (warp == T::W_PROD) {
     // ================================================================ TMA producer
-    TileProducer<T> prod;
-    prod.init(&p, &kmap, &vmap, smem, full, empty, qfull, abort_flag, lane, it_begin, it_end);
-    prod.fill(0xFFFFFFFFu);  // every tile of the work list, as stages come free
+    TcProducer<T> prod;
+    prod.init(&p, &kmap, &vmap, smem, full_k, empty_k, full_v, empty_v, abort_flag, lane,
+              it_begin, it_end);
+    prod.run();  // every tile of the work list, as slots come free
     prod.drain();
   } else if (warp == T::W_MMA) {
     // ================================================================ MMA issue
     if (lane == 0) {
-      uint32_t g = 0, tile_ctr = 0, items_done = 0;
-      uint32_t q_ph = 0, o_ph = 0, pf_ph[2] = {0, 0}, sfree_ph[2] = {0, 0}, cvf_ph[2] = {0, 0};
-      // O += P V of step gp (P of that step, in buffer gp % 2, must be written)
-      auto issue_pv = [&](uint32_t gp, uint32_t vaddr, bool first, int stage, bool last) {
-        wait_bar(&p_full[gp & 1], pf_ph[gp & 1]);
-        pf_ph[gp & 1] ^= 1u;
+      uint32_t g = 0, items_done = 0;
+      uint32_t q_ph = 0, o_ph = 0;
+      // step x uses buffer x % NSP; every barrier of a buffer completes once per use, in
+      // step order, so the phase of step x is (x / NSP) & 1
+      // O += P V of step gp (its P, in buffer gp % 2, must be written); the commit releases
+      // the V slot
+      auto issue_pv = [&](uint32_t gp, bool first) {
+        const int slot = (int)(gp % T::NSTAGE);
+        const uint32_t vaddr = smem_addr(smem + T::OFF_V + slot * T::KTILE);
+        wait_bar(&full_v[slot], (gp / T::NSTAGE) & 1);
+        wait_bar(&p_full[gp % T::NSP], (gp / T::NSP) & 1);
         if (first && items_done > 0) {  // the previous item's epilogue has read O
           wait_bar(o_free, o_ph);
           o_ph ^= 1u;
         }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < T::SUB / 16; ++kk) {
+        for (int kk = 0; kk < SUB / 16; ++kk) {
           const uint64_t bd = umma_desc(vaddr + kk * 2048, T::KSLAB, 1024);
-          umma_f16_ta(t_o, t_p + (gp & 1) * (T::SUB / 2) + kk * 8, bd, ID_PV, !(first && kk == 0));
+          umma_f16_ta(t_o, t_s + (gp % T::NSP) * SUB + kk * 8, bd, ID_PV, !(first && kk == 0));
         }
-        umma_commit(&pv_done[gp & 1]);
-        if constexpr (T::FP8) {
-          umma_commit(&cv_free[gp & 1]);
-        } else {
-          if (last) umma_commit(&empty[stage]);  // the stage's K and V are read
-        }
+        umma_commit(&pv_done[gp % T::NSP]);
+        umma_commit(&empty_v[slot]);
       };
       for (int it = it_begin; it < it_end; ++it) {
         const int4 item = p.items[it];
         const int t0 = item.y, t1 = item.z;
         if (t1 <= t0) continue;
-        const int nsub = ceil_div(t1 - t0, T::SUB);
-        wait_bar(q_full, q_ph);  // the item's query tile is in shared memory
+        const int nsub = ceil_div(t1 - t0, SUB);
+        wait_bar(q_full, q_ph);  // the item's query rows are in tensor memory
         q_ph ^= 1u;
-        uint32_t pv_vaddr = 0, pv_g = 0;
-        int pv_stage = 0;
-        bool pv_last = false;
-        int stage = 0;
+        // the PVs trail the S MMAs by LAG steps, so the in-order tensor pipe always holds
+        // the logits of the next steps ahead of a PV that waits for the softmax
+        constexpr int LAG = T::NSP - 1;
+        const uint32_t g_item = g;  // the item's first step
         for (int j = 0; j < nsub; ++j, ++g) {
-          const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB, T::SUB);
-          if (q.c0 == 0) {
-            stage = tile_ctr % T::NSTAGE;
-            if constexpr (!T::FP8) wait_bar(&full[stage], (tile_ctr / T::NSTAGE) & 1);
-            ++tile_ctr;
-          }
-          uint32_t kbase, vaddr;
-          if constexpr (T::FP8) {
-            wait_bar(&cv_full[g & 1], cvf_ph[g & 1]);
-            cvf_ph[g & 1] ^= 1u;
-            kbase = smem_addr(scv + (g & 1) * T::CV_BUF);
-            vaddr = kbase + 2 * T::CV_SLAB;
-          } else {
-            kbase = smem_addr(smem + stage * T::STAGE) + q.c0 * 128;
-            vaddr = smem_addr(smem + stage * T::STAGE + T::KTILE) + q.c0 * 128;
-          }
-          if (g >= 2) {  // the softmax has loaded the logits of step g - 2 from this buffer
-            wait_bar(&s_free[g & 1], sfree_ph[g & 1]);
-            sfree_ph[g & 1] ^= 1u;
+          const int slot = (int)(g % T::NSTAGE);
+          wait_bar(&full_k[slot], (g / T::NSTAGE) & 1);
+          const uint32_t kbase = smem_addr(smem + T::OFF_K + slot * T::KTILE);
+          if (g >= (uint32_t)T::NSP) {  // the buffer holds P(g - NSP) until its PV has read it
+            const uint32_t x = g - T::NSP;
+            wait_bar(&pv_done[x % T::NSP], (x / T::NSP) & 1);
           }
           tc_fence_after();
-          const uint32_t t_sg = t_s + (g & 1) * T::SUB;
+          const uint32_t t_sg = t_s + (g % T::NSP) * SUB;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t bd = umma_desc(kbase + (kk >> 2) * T::KSLAB + (kk & 3) * 32, 16, 1024);
             umma_f16_ta(t_sg, t_q + kk * 8, bd, ID_S, kk > 0);
           }
-          umma_commit(&s_full[g & 1]);
-          if (j > 0) issue_pv(pv_g, pv_vaddr, j == 1, pv_stage, pv_last);
-          pv_g = g;
-          pv_vaddr = vaddr;
-          pv_stage = stage;
-          pv_last = q.last;
+          umma_commit(&s_full[g % T::NSP]);
+          umma_commit(&empty_k[slot]);
+          if (j >= LAG) issue_pv(g - LAG, j == LAG);
         }
-        issue_pv(pv_g, pv_vaddr, nsub == 1, pv_stage, pv_last);
+        for (int j = nsub > LAG ? nsub - LAG : 0; j < nsub; ++j) issue_pv(g_item + j, j == 0);
         ++items_done;
       }
       umma_commit(mma_end);
       if (!mbar_wait_drain(mma_end, 0)) atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
     }
-  } else if (warp < T::W_CONV) {
+  } else {
     // ================================================================ softmax and epilogue
     const int stid = tid - T::W_SOFT * 32;            // 0 .. 127 over the four warps
     const int r = 32 * (warp & 3) + lane;            // query row = this thread's TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const bool tensor_scale = p.scale_mode == PA_SCALE_PER_TENSOR;
-    const float kts = tensor_scale ? __ldg(p.k_scale) : 1.f;
-    const float vts = tensor_scale ? __ldg(p.v_scale) : 1.f;
-    const float qk_scale = p.qk_scale * kts;
-    uint32_t g = 0, sfull_ph[2] = {0, 0}, sc_ph[2] = {0, 0};
-    uint32_t pv_seen[2] = {0, 0};  // completions of pv_done[b] consumed so far
-    // wait until the PV of step x (which read P buffer x % 2) has completed; each buffer's
-    // completions are consumed in order, and none is ever two ahead of its consumer
+    const float qk_scale = p.qk_scale;
+    const float vts = 1.f;
+    uint32_t g = 0;
+    uint32_t pv_next = 0;  // the first step whose PV completion is not consumed yet
+    // wait until the PV of step x (which read buffer x % NSP) has completed; completions
+    // are consumed in step order, and none is ever two ahead of its consumer on a buffer
     auto wait_pv_step = [&](uint32_t x) {
-      const uint32_t bx = x & 1, ux = x >> 1;
-      while (pv_seen[bx] <= ux) {
-        wait_bar(&pv_done[bx], pv_seen[bx] & 1);
-        ++pv_seen[bx];
-      }
+      for (; pv_next <= x; ++pv_next)
+        wait_bar(&pv_done[pv_next % T::NSP], (pv_next / T::NSP) & 1);
       tc_fence_after();
     };
-    uint32_t tile_base = 0;  // tiles of the earlier items (ring position of this item's first)
     int2 pend_even = make_int2(-1, 0), pend_odd = make_int2(-1, 0);  // held by stid 0
     int4 item_next = it_begin < it_end ? p.items[it_begin] : make_int4(0, 0, 0, -1);
     for (int it = it_begin; it < it_end; ++it) {
@@ -463,7 +537,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       const int n = __ldg(p.ctx + b), ql = __ldg(p.qlens + b);
       const int2 uinfo = slot >= 0 ? __ldg(&p.unit_info[u]) : make_int2(0, 1);
       const bool in_dec = slot >= 0 && uinfo.y <= p.ns_dec;
-      const int nsub = ceil_div(t1 - t0, T::SUB);
+      const int nsub = ceil_div(t1 - t0, SUB);
       int cnt_seen = -1;
       const int rg = rb * MP + r;
       const bool real = r < MP && rg < p.M;
@@ -479,16 +553,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
           uint32_t w[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            uint4 v = real ? __ldg(qrow + 8 * h + c) : make_uint4(0, 0, 0, 0);
-            if constexpr (T::FP8 && QK == Q_BF16) {  // f16 operands for an fp8 cache
-              uint32_t t4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int jw = 0; jw < 4; ++jw) {
-                const float2 f = bf16x2_to_f2(t4[jw]);
-                t4[jw] = pack16x2<false>(f.x, f.y);
-              }
-              v = make_uint4(t4[0], t4[1], t4[2], t4[3]);
-            }
+            const uint4 v = real ? __ldg(qrow + 8 * h + c) : make_uint4(0, 0, 0, 0);
             w[4 * c] = v.x;
             w[4 * c + 1] = v.y;
             w[4 * c + 2] = v.z;
@@ -504,48 +569,32 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
 
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nsub; ++j, ++g) {
-        const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB, T::SUB);
+        const int tok0 = t0 + j * SUB, nv = min(SUB, t1 - tok0);  // tokens of the item here
         if (in_dec && j + 1 == nsub && stid == 0) cnt_seen = ld_acquire_gpu(&p.unit_cnt[u]);
-        if (!T::FP8 && q.n < T::SUB) {
-          // the zeroing below writes into the ring stage: the tile must have landed (the
-          // MMA warp has waited for it; this wait is for the ordering of the writes)
-          const uint32_t tc = tile_base + (uint32_t)(j / T::NSUB);
-          wait_bar(&full[tc % T::NSTAGE], (tc / T::NSTAGE) & 1);
+        if (nv < SUB) {
+          // the zeroing below writes into the V slot: the tile must have landed (this wait
+          // orders the writes after the copy)
+          wait_bar(&full_v[g % T::NSTAGE], (g / T::NSTAGE) & 1);
         }
-        wait_bar(&s_full[g & 1], sfull_ph[g & 1]);
-        sfull_ph[g & 1] ^= 1u;
+        wait_bar(&s_full[g % T::NSP], (g / T::NSP) & 1);
         tc_fence_after();
+        const uint32_t t_sg = t_s + (g % T::NSP) * SUB + lane_off;
         float x[SUB];
-        if constexpr (SUB == 64)
-          tmem_ld64(t_s + (g & 1) * SUB + lane_off, x);
-        else
-          tmem_ld32(t_s + (g & 1) * SUB + lane_off, x);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[g & 1]);
-        const float* ksc = nullptr;
-        const float* vsc = nullptr;
-        if constexpr (TOKS) {
-          wait_bar(&sc_full[g & 1], sc_ph[g & 1]);
-          sc_ph[g & 1] ^= 1u;
-          ksc = ssc + (g & 1) * 2 * T::SUB;
-          vsc = ksc + T::SUB;
-        }
+        tmem_ld64(t_sg, x);
         // ---- online softmax of this thread's row (log2 units), two logits per instruction
         const float2 s2 = make_float2(qk_scale, qk_scale), z2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < SUB / 2; ++i) {
-          float2 y = ffma2(make_float2(x[2 * i], x[2 * i + 1]), s2, z2);
-          if constexpr (TOKS) y = ffma2(y, make_float2(ksc[2 * i], ksc[2 * i + 1]), z2);
+          const float2 y = ffma2(make_float2(x[2 * i], x[2 * i + 1]), s2, z2);
           x[2 * i] = y.x;
           x[2 * i + 1] = y.y;
         }
         // masked keys (past the item's tokens or past the row's causal limit) become -inf;
         // most steps have none
-        if (q.n < T::SUB || q.tok0 + q.c0 + T::SUB > lim) {
+        if (nv < SUB || tok0 + SUB > lim) {
 #pragma unroll
           for (int jj = 0; jj < SUB; ++jj)
-            if (jj >= q.n || q.tok0 + q.c0 + jj >= lim) x[jj] = -INFINITY;
+            if (jj >= nv || tok0 + jj >= lim) x[jj] = -INFINITY;
         }
         float mx = -INFINITY;
 #pragma unroll
@@ -555,35 +604,36 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         const float mn = need ? mx : m_run;
         const float alpha = (mn == m_run || m_run == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
         m_run = mn;
-        // this thread's row of P, packed: 64 tokens = eight 16-byte chunks; a masked logit
-        // (-inf) gives exp2 = 0, and a row with no visible key so far has only zeros
+        if (g >= (uint32_t)T::NSP) wait_pv_step(g - T::NSP);  // (complete: S(g) came after it)
+        // this thread's row of P, 16-bit pairs over the first SUB / 2 columns of its own
+        // logits (all of them are in registers); a masked logit (-inf) gives exp2 = 0, and a
+        // row with no visible key so far has only zeros
         float lsum = 0.f;
-        uint32_t pk[SUB / 2];
-        if (m_run == -INFINITY) {
-#pragma unroll
-          for (int i = 0; i < SUB / 2; ++i) pk[i] = 0u;
-        } else {
-          const float2 nm = make_float2(-m_run, -m_run), one2 = make_float2(1.f, 1.f);
+        {
+          const float2 nm = make_float2(m_run == -INFINITY ? 0.f : -m_run,
+                                        m_run == -INFINITY ? 0.f : -m_run);
+          const float2 one2 = make_float2(1.f, 1.f);
           float2 ls2 = z2;
 #pragma unroll
-          for (int i = 0; i < SUB / 2; ++i) {
-            const float2 t = ffma2(make_float2(x[2 * i], x[2 * i + 1]), one2, nm);
-            float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
-            ls2 = ffma2(make_float2(p0, p1), one2, ls2);
-            if constexpr (TOKS) {  // a masked token's scale slot may be stale
-              p0 = p0 > 0.f ? p0 * vsc[2 * i] : 0.f;
-              p1 = p1 > 0.f ? p1 * vsc[2 * i + 1] : 0.f;
+          for (int h = 0; h < SUB / 32; ++h) {  // 32 tokens = 16 columns at a time
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 t = ffma2(make_float2(x[32 * h + 2 * i], x[32 * h + 2 * i + 1]), one2, nm);
+              const float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
+              ls2 = ffma2(make_float2(p0, p1), one2, ls2);
+              pk[i] = pack16x2<BF>(p0, p1);
             }
-            pk[i] = pack16x2<BF>(p0, p1);
+            tmem_st16u(t_sg + 16 * h, pk);
           }
           lsum = ls2.x + ls2.y;
         }
         l_run = l_run * alpha + lsum;
         if (rescale && j > 0) {
           // O holds earlier tokens of this item: scale this warp's rows once every PV into
-          // O has completed
+          // O has completed (the PV of this step waits for p_full below)
           wait_pv_step(g - 1);
-#pragma unroll
+#pragma unroll 1
           for (int h = 0; h < D / 32; ++h) {
             float o[32];
             tmem_ld32(t_o + lane_off + 32 * h, o);
@@ -591,34 +641,25 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
             for (int jj = 0; jj < 32; ++jj) o[jj] *= alpha;
             tmem_st32(t_o + lane_off + 32 * h, o);
           }
-          tmem_wait_st();
         }
-        if (g >= 2) wait_pv_step(g - 2);  // P buffer g % 2 was last read by the PV of step g - 2
-        tmem_st_p<SUB / 2>(t_p + (g & 1) * (SUB / 2) + lane_off, pk);
         tmem_wait_st();
-        if constexpr (!T::FP8) {
-          if (q.n < T::SUB) {
-            // value rows past the item's tokens may hold anything: zero them (before this
-            // step's PV reads them) so that zero weights stay zero
-            const int stage = (int)(tile_base + (uint32_t)(j / T::NSUB)) % T::NSTAGE;
-            char* vt = smem + stage * T::STAGE + T::KTILE;
-            for (int e = stid; e < (T::SUB - q.n) * T::NSLAB * 8; e += 128) {
-              const int rr = q.n + e / (T::NSLAB * 8), sl = (e / 8) % T::NSLAB, c = e & 7;
-              *reinterpret_cast<uint4*>(vt + sl * (T::TT * 128) + sw128_chunk(q.c0 + rr, c)) =
-                  make_uint4(0, 0, 0, 0);
-            }
+        if (nv < SUB) {
+          // value rows past the item's tokens may hold anything: zero them (before this
+          // step's PV reads them) so that zero weights stay zero
+          char* vt = smem + T::OFF_V + (g % T::NSTAGE) * T::KTILE;
+          for (int e = stid; e < (SUB - nv) * T::NSLAB * 8; e += 128) {
+            const int rr = nv + e / (T::NSLAB * 8), sl = (e / 8) % T::NSLAB, c = e & 7;
+            *reinterpret_cast<uint4*>(vt + sl * T::KSLAB + sw128_chunk(rr, c)) =
+                make_uint4(0, 0, 0, 0);
           }
         }
         fence_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[g & 1]);
+        if (lane == 0) mbar_arrive(&p_full[g % T::NSP]);
       }
-      tile_base += (uint32_t)ceil_div(t1 - t0, T::TT);
-
       // ---- epilogue: O of this thread's row from tensor memory, in two halves of 64 dims
-      if (g >= 2) wait_pv_step(g - 2);  // the item's last two PVs (in order)
-      wait_pv_step(g - 1);
+      wait_pv_step(g - 1);  // every PV of the item (in order)
       if (stid == 0) *cnt_seen_s = cnt_seen;
       named_barrier_sync(SOFT_BAR, 128);
       const bool fin = in_dec && slot == uinfo.x && *cnt_seen_s == uinfo.y - 1;
@@ -704,66 +745,11 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       pend[2] = pend_odd.x;
       pend[3] = pend_odd.y;
     }
-  } else {
-    // ================================================================ fp8 widening
-    if constexpr (T::FP8) {
-      const int ctid = tid - T::W_CONV * 32;  // 0 .. 63
-      uint32_t g = 0, tile_ctr = 0, cvfree_ph[2] = {0, 0};
-      int stage = 0;
-      for (int it = it_begin; it < it_end; ++it) {
-        const int4 item = p.items[it];
-        const int t0 = item.y, t1 = item.z;
-        if (t1 <= t0) continue;
-        const int nsub = ceil_div(t1 - t0, T::SUB);
-        for (int j = 0; j < nsub; ++j, ++g) {
-          const TcStep q = tc_step(t0, t1, j, T::TT, T::NSUB, T::SUB);
-          if (q.c0 == 0) {
-            stage = tile_ctr % T::NSTAGE;
-            wait_bar(&full[stage], (tile_ctr / T::NSTAGE) & 1);
-            ++tile_ctr;
-          }
-          if (g >= 2) {  // the PV of step g - 2 has read this buffer
-            wait_bar(&cv_free[g & 1], cvfree_ph[g & 1]);
-            cvfree_ph[g & 1] ^= 1u;
-          }
-          const char* st = smem + stage * T::STAGE;
-          char* cv = scv + (g & 1) * T::CV_BUF;
-          for (int e = ctid; e < 2 * T::SUB * 8; e += 32 * T::NCW) {
-            const int kv = e / (T::SUB * 8), rr = (e / 8) % T::SUB, c = e & 7;
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-            if (rr < q.n) {  // rows past the item's tokens become zero
-              const uint4 w = *reinterpret_cast<const uint4*>(st + kv * T::KTILE + sw128_chunk(q.c0 + rr, c));
-              lo = make_uint4(e4m3x2_to_h2(w.x), e4m3x2_to_h2(w.x >> 16), e4m3x2_to_h2(w.y),
-                              e4m3x2_to_h2(w.y >> 16));
-              hi = make_uint4(e4m3x2_to_h2(w.z), e4m3x2_to_h2(w.z >> 16), e4m3x2_to_h2(w.w),
-                              e4m3x2_to_h2(w.w >> 16));
-            }
-            // dims 16c .. 16c + 15 -> 16-bit slab c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1
-            char* dst = cv + kv * (2 * T::CV_SLAB) + (c >> 2) * T::CV_SLAB;
-            *reinterpret_cast<uint4*>(dst + sw128_chunk(rr, 2 * (c & 3))) = lo;
-            *reinterpret_cast<uint4*>(dst + sw128_chunk(rr, 2 * (c & 3) + 1)) = hi;
-          }
-          if constexpr (TOKS) {  // the scales leave the stage with the rows
-            const float* sks = reinterpret_cast<const float*>(st + 2 * T::KTILE);
-            float* sc = ssc + (g & 1) * 2 * T::SUB;
-            sc[ctid] = sks[q.c0 + ctid];
-            sc[T::SUB + ctid] = sks[T::TT + q.c0 + ctid];
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&cv_full[g & 1]);
-            if constexpr (TOKS) mbar_arrive(&sc_full[g & 1]);
-            if (q.last) mbar_arrive(&empty[stage]);  // this warp is done with the stage
-          }
-        }
-      }
-    }
   }
 
   tc_fence_before();
   __syncthreads();  // every role is done: no copy or MMA in flight
-  if (warp >= T::W_SOFT && warp < T::W_CONV) {
+  if (warp >= T::W_SOFT) {
     const int stid = tid - T::W_SOFT * 32;
     finish_pending<D, MP, QK, 4>(p, pend, reinterpret_cast<float*>(smem), T::STAGE / 4, mlbuf, stid);
     zero_empty_units<D, MP, QK, 128>(p, stid);

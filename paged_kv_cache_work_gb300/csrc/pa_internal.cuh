@@ -45,6 +45,9 @@ struct Variant {
 constexpr int kSimtMaxRows = 8;
 // Bytes of one K (or V) tile of a stage.
 constexpr int kTileBytes = 16384;
+// Tokens of one tile of the tcgen05 kernel (one MMA step: 16 KB of K at head dim 128, 32 KB
+// at 256).
+constexpr int kTcStepTokens = 64;
 // Fixed cost of a work item, in tiles of streaming: a CTA that starts a unit pays for the
 // unit's epilogue and for refilling its copy pipeline (about 5 us at the ~22 GB/s one CTA
 // streams, or three tiles of K and V), so the planner counts every unit that long.
@@ -102,8 +105,9 @@ inline Variant make_variant(const pa_config& c) {
   else
     v.mp = v.rows <= kSimtMaxRows ? pow2_at_least(v.rows) : kSimtMaxRows;
   v.rb = ceil_div(v.rows, v.mp);
-  v.tt = kTileBytes / (c.head_dim * v.bpe);
-  v.item_cost = kItemCostTiles * v.tt;
+  v.tt = v.path == 2 ? kTcStepTokens : kTileBytes / (c.head_dim * v.bpe);
+  // the item cost is measured in 16 KB tiles of streaming, rounded up to whole tiles
+  v.item_cost = round_up(kItemCostTiles * (kTileBytes / (c.head_dim * v.bpe)), v.tt);
   v.units = c.batch * c.num_kv_heads * v.rb;
   const int kvk = c.kv_dtype == PA_FP8_E4M3 ? 2 : (c.kv_dtype == PA_FP16 ? 1 : 0);
   const bool toks = c.kv_scale_mode == PA_SCALE_PER_TOKEN;

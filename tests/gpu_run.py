@@ -66,6 +66,7 @@ def _pow2_at_least(x):
 
 SIMT_MAX_ROWS = 8
 TILE_BYTES = 16384
+TC_STEP_TOKENS = 64
 ITEM_COST_TILES = 3
 TC_MIN_ROWS = 33
 DECODE_MERGE_PIECES = 2
@@ -83,17 +84,19 @@ def decode_merge_limit(split_merge: int) -> int:
 def variant(cfg: pa.PaConfig, ctas: int):
     rows = (cfg.num_q_heads // cfg.num_kv_heads) * cfg.max_q_len
     bpe = 1 if cfg.kv_dtype == pa.FP8_E4M3 else 2
-    if bpe == 2 and cfg.head_dim >= 128 and rows >= TC_MIN_ROWS:  # tcgen05
+    tc = bpe == 2 and cfg.head_dim >= 128 and rows >= TC_MIN_ROWS
+    if tc:  # tcgen05
         mp = 64 if rows <= 64 else 128
     elif cfg.head_dim * bpe >= 128:  # mma.sync kernel
         mp = 64 if rows >= 64 else (16 if rows <= 16 else _pow2_at_least(rows))
     else:
         mp = _pow2_at_least(rows) if rows <= SIMT_MAX_ROWS else SIMT_MAX_ROWS
     rb = -(-rows // mp)
-    tt = TILE_BYTES // (cfg.head_dim * bpe)
+    tt = TC_STEP_TOKENS if tc else TILE_BYTES // (cfg.head_dim * bpe)
+    cost = ITEM_COST_TILES * (TILE_BYTES // (cfg.head_dim * bpe))
     return dict(rows=rows, mp=mp, rb=rb, tt=tt, units=cfg.batch * cfg.num_kv_heads * rb,
                 ctas=ctas, ns_dec=decode_merge_limit(cfg.split_merge),
-                item_cost=ITEM_COST_TILES * tt)
+                item_cost=-(-cost // tt) * tt)
 
 
 def layout(cfg: pa.PaConfig, v: dict):
