@@ -52,14 +52,15 @@ KERNEL_SOURCES = ["paged_kv_cache_work_gb300/csrc/decode_simt.cuh",
 
 def decode_shape(wl):
     """(decode kernel name, rows per unit) the library picks for a workload: a 16-bit cache
-    with head dim 128 or 256 and more than 32 query rows per kv head goes to the tcgen05 kernel in
-    tiles of 64 or 128 rows; other caches with a tile row of at least 128 bytes to the
-    mma.sync kernel in tiles of 16, 32 or 64 rows; the rest (64-dim fp8) to the CUDA-core
-    kernel."""
+    with head dim 128 or 256, or an fp8 cache with head dim 128 and per-tensor or no scales,
+    and more than 32 query rows per kv head goes to the tcgen05 kernel in tiles of 64 or 128
+    rows; other caches with a tile row of at least 128 bytes to the mma.sync kernel in tiles
+    of 16, 32 or 64 rows; the rest (64-dim fp8) to the CUDA-core kernel."""
     rows = (wl.num_q_heads // wl.num_kv_heads) * wl.max_q_len
     bpe = 1 if wl.kv_dtype == "fp8" else 2
     pow2 = 1 << max(0, (rows - 1).bit_length())
-    if wl.head_dim >= 128 and rows >= 33 and bpe == 2:
+    tc_fp8 = wl.head_dim == 128 and wl.scale_mode != "token"
+    if wl.head_dim >= 128 and rows >= 33 and (bpe == 2 or tc_fp8):
         return "decode_tc_kernel", 64 if rows <= 64 else 128
     if wl.head_dim * bpe >= 128:
         return "decode_mma_kernel", 64 if rows >= 64 else max(16, pow2)

@@ -7,10 +7,13 @@
 //               96 KB each: a K slot is released by the S that read it and a V slot by its
 //               PV, and K is copied one step ahead of V;
 //   warp 1      one thread issues, per step g, S = Q K^T (M = 128, N = 64, K = head dim)
-//               into tensor-memory buffer g % NSP, and then O += P V for step
-//               g - (NSP - 1) (M = 128, N = head dim, K = 64, V read as an MN-major
-//               operand), so the in-order tensor pipe holds the next logits ahead of any
-//               PV that waits for the softmax;
+//               into tensor-memory buffer g % NSP, and then O += P V for step g - LAG
+//               (M = 128, N = head dim, K = 64, V read as an MN-major operand), so the
+//               in-order tensor pipe holds the next logits ahead of any PV that waits for
+//               the softmax;
+//   warps 6-7   (fp8 caches, per-tensor or no scales) widen each step's e4m3 K rows to
+//               f16 in one of three shared-memory buffers, released by the step's S, and
+//               its V rows in one of four, released by its PV;
 //   warps 2-5   one query row per thread: load the row's logits with tcgen05.ld, online
 //               softmax in registers (a row never leaves its thread), write the row of P as
 //               16-bit pairs over the first half of the same logits buffer; at the end of an
@@ -38,29 +41,40 @@ struct TcTraits {
   static constexpr int KVK = KVK_;
   static constexpr bool TOKS = TOKS_;
   static constexpr bool FP8 = KVK == KV_FP8;
-  static constexpr int BPE = 2;
-  static constexpr int W_PROD = 0, W_MMA = 1, W_SOFT = 2;
-  static constexpr int NW = 6;
+  static constexpr int BPE = FP8 ? 1 : 2;
+  static constexpr int W_PROD = 0, W_MMA = 1, W_SOFT = 2, W_CONV = 6;
+  static constexpr int NCW = FP8 ? 2 : 0;  // warps that widen fp8 tiles to f16
+  static constexpr int NW = 6 + NCW;
   static constexpr int NTHREADS = NW * 32;
   static constexpr int TT = kTcStepTokens;  // tokens per tile and per MMA step: 64
   static constexpr int SUB = TT;
-  static constexpr int KTILE = TT * D * BPE;         // 16 KB, or 32 KB at head dim 256
-  static constexpr int NSTAGE = 98304 / KTILE;       // slots of each ring: 6, or 3 (96 KB)
+  static constexpr int KTILE = TT * D * BPE;  // 16 KB, 32 KB at head dim 256, 8 KB for fp8
+  static constexpr int SLOT = KTILE;  // a ring slot
+  static constexpr int NSTAGE = FP8 ? 5 : 98304 / KTILE;  // slots of each ring: 6, 3 or 5
   static constexpr int ROWB = 128;             // swizzled slabs of 128 bytes per row
   static constexpr int NSLAB = D * BPE / 128;  // slabs of a cache tile row
   // S/P buffers in tensor memory: four at head dim 128 (S(g) waits only for the PV of
   // step g - 4), two at 256
   static constexpr int NSP = D == 128 ? 4 : 2;
-  static constexpr int OFF_K = 0;                       // K ring: NSTAGE tiles
-  static constexpr int OFF_V = OFF_K + NSTAGE * KTILE;  // V ring: NSTAGE tiles
-  static constexpr int STAGE = 2 * KTILE;               // (scratch capacity at the end)
-  static constexpr int KSLAB = TT * 128;                // slab stride of the K and V operands
-  static constexpr int OFF_ML = OFF_V + NSTAGE * KTILE;
+  static constexpr int OFF_K = 0;                      // K ring: NSTAGE slots
+  static constexpr int OFF_V = OFF_K + NSTAGE * SLOT;  // V ring: NSTAGE slots
+  // fp8: the widened (f16) K rows of NCK steps and V rows of NCV steps, each a
+  // 128-byte-swizzled operand of two 64-dim slabs (a K buffer is released by its S, a V
+  // buffer by its PV)
+  static constexpr int NCK = FP8 ? 3 : 0;
+  static constexpr int NCV = FP8 ? 4 : 0;
+  static constexpr int CV_SLAB = SUB * 128;
+  static constexpr int CV_BUF = 2 * CV_SLAB;
+  static constexpr int OFF_CV = OFF_V + NSTAGE * SLOT;  // K buffers, then V buffers
+  static constexpr int SCRATCH = OFF_CV;  // bytes free for the merges at the end (the rings)
+  static constexpr int LAG = NSP - 1;  // steps a PV trails its S
+  static constexpr int KSLAB = FP8 ? CV_SLAB : TT * 128;  // slab stride of the MMA operands
+  static constexpr int OFF_ML = OFF_CV + (NCK + NCV) * CV_BUF;
   static constexpr int ML_BYTES = round_up(2 * MP * 4, 128);
   static constexpr int OFF_BAR = round_up(OFF_ML + ML_BYTES, 64);
   // full_k, empty_k, full_v, empty_v (NSTAGE each), s_full, p_full, pv_done (NSP each),
-  // o_free, q_full, mma_end
-  static constexpr int NBAR = 4 * NSTAGE + 3 * NSP + 3;
+  // o_free, q_full, mma_end, full and free of the K buffers and of the V buffers
+  static constexpr int NBAR = 4 * NSTAGE + 3 * NSP + 3 + 2 * (NCK + NCV);
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 16 + 1024;
   static constexpr int CTAS_PER_SM = 1;
   // Tensor memory (lane = query row, 32-bit columns): NSP S/P buffers of SUB fp32 columns
@@ -71,7 +85,13 @@ struct TcTraits {
   static constexpr uint32_t COL_O = D == 256 ? 256 : NSP * SUB;
   static constexpr uint32_t COL_Q = D == 256 ? NSP * SUB : COL_O + D;
   static_assert(NSP * SUB + D + D / 2 <= (int)TMEM_COLS, "tensor memory");
-  static_assert(!FP8 && !TOKS, "16-bit caches only");
+  static_assert(!TOKS, "per-token scales stay on the mma.sync kernel");
+  static_assert(!FP8 || D == 128, "fp8 caches at head dim 128");
+  static_assert(!FP8 || (SUB * 8) % (32 * NCW) == 0, "widening: whole passes");
+  // the V rows of step g wait for the PV of step g - NCV, issued after the S of step
+  // g - NCV + LAG, which waits for the K rows of that step: the widening, K(g) then V(g),
+  // must not need K rows past g
+  static_assert(LAG < NSP && (!FP8 || LAG <= NCV), "no cycle between the roles");
   static_assert(MP == 64 || MP == 128, "row tile");
   static_assert(D == 128 || D == 256, "head dim");
   static_assert(SUB == 64, "step");
@@ -206,6 +226,12 @@ __device__ __forceinline__ uint32_t pack16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
   }
 }
+// Two E4M3 codes (low byte first) to an f16 pair (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t w) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
 // 32 lanes x 32 bits x 64 columns: thread t of warp w gets columns [col, col + 64) of lane
 // 32 (w % 4) + t, with one wait.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -325,12 +351,12 @@ struct TcProducer {
     }
     if (lane == 0) mbar_arrive_expect_tx(&full[s], bx.nvalid * box_bytes);
     __syncwarp();
+    char* slot = smem + ring + s * T::SLOT;
     if (bx.ok) {
       // slab h of page j lands at h * (TT rows) + j * (box rows), in units of ROWB bytes
       const int page = lane / T::NSLAB, slab = lane % T::NSLAB;
       const uint32_t dst = (uint32_t)(slab * T::TT + page * box_rows) * T::ROWB;
-      tma_load_4d(smem + ring + s * T::KTILE + dst, map, &full[s], slab * (T::ROWB / T::BPE),
-                  bx.g, bx.row, bx.blk);
+      tma_load_4d(slot + dst, map, &full[s], slab * (T::ROWB / T::BPE), bx.g, bx.row, bx.blk);
     }
     return true;
   }
@@ -369,7 +395,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   using T = TcTraits<D_, MP, KVK, TOKS>;
   constexpr int SUB = T::SUB;
   constexpr int D = T::D;
-  constexpr bool BF = KVK == KV_BF16;  // MMA operands bf16 (else f16)
+  constexpr bool BF = KVK == KV_BF16;  // MMA operands bf16 (else f16: f16 and fp8 caches)
   constexpr uint32_t ID_S = umma_idesc(128, SUB, BF, false);
   constexpr uint32_t ID_PV = umma_idesc(128, D, BF, true);
   constexpr int SOFT_BAR = 2;  // named barrier of the four softmax warps
@@ -385,7 +411,11 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   uint64_t* o_free = pv_done + T::NSP;
   uint64_t* q_full = o_free + 1;
   uint64_t* mma_end = q_full + 1;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_end + 1);
+  uint64_t* ck_full = mma_end + 1;       // [NCK]: widened K rows of the step in buffer b
+  uint64_t* ck_free = ck_full + T::NCK;  // [NCK]: the S that read buffer b has completed
+  uint64_t* cv_full = ck_free + T::NCK;  // [NCV]: widened V rows of the step in buffer b
+  uint64_t* cv_free = cv_full + T::NCV;  // [NCV]: the PV that read buffer b has completed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(cv_free + T::NCV);
   volatile int* pend = abort_flag + 2;        // [4]: split pieces published, see finish_pending
   volatile int* cnt_seen_s = abort_flag + 6;  // published pieces of the item's unit, seen late
   uint32_t* tslot = reinterpret_cast<uint32_t*>(const_cast<int*>(abort_flag + 7));
@@ -394,10 +424,19 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < T::NSTAGE; ++s) {
-      mbar_init(&full_k[s], 1);
-      mbar_init(&empty_k[s], 1);  // the commit of the S that read the slot
+      mbar_init(&full_k[s], 1);  // the expect_tx arrival of the copy
       mbar_init(&full_v[s], 1);
-      mbar_init(&empty_v[s], 1);  // the commit of the PV that read the slot
+      // readers: the commit of the S (K) or PV (V) that read the slot, or the fp8 widening
+      mbar_init(&empty_k[s], T::FP8 ? T::NCW : 1);
+      mbar_init(&empty_v[s], T::FP8 ? T::NCW : 1);
+    }
+    for (int b = 0; b < T::NCK; ++b) {
+      mbar_init(&ck_full[b], T::NCW);
+      mbar_init(&ck_free[b], 1);
+    }
+    for (int b = 0; b < T::NCV; ++b) {
+      mbar_init(&cv_full[b], T::NCW);
+      mbar_init(&cv_free[b], 1);
     }
     for (int b = 0; b < T::NSP; ++b) {
       mbar_init(&s_full[b], 1);
@@ -458,8 +497,14 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       // the V slot
       auto issue_pv = [&](uint32_t gp, bool first) {
         const int slot = (int)(gp % T::NSTAGE);
-        const uint32_t vaddr = smem_addr(smem + T::OFF_V + slot * T::KTILE);
-        wait_bar(&full_v[slot], (gp / T::NSTAGE) & 1);
+        uint32_t vaddr;
+        if constexpr (T::FP8) {
+          wait_bar(&cv_full[gp % T::NCV], (gp / T::NCV) & 1);
+          vaddr = smem_addr(smem + T::OFF_CV + (T::NCK + gp % T::NCV) * T::CV_BUF);
+        } else {
+          vaddr = smem_addr(smem + T::OFF_V + slot * T::SLOT);
+          wait_bar(&full_v[slot], (gp / T::NSTAGE) & 1);
+        }
         wait_bar(&p_full[gp % T::NSP], (gp / T::NSP) & 1);
         if (first && items_done > 0) {  // the previous item's epilogue has read O
           wait_bar(o_free, o_ph);
@@ -472,7 +517,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
           umma_f16_ta(t_o, t_s + (gp % T::NSP) * SUB + kk * 8, bd, ID_PV, !(first && kk == 0));
         }
         umma_commit(&pv_done[gp % T::NSP]);
-        umma_commit(&empty_v[slot]);
+        if constexpr (T::FP8)
+          umma_commit(&cv_free[gp % T::NCV]);
+        else
+          umma_commit(&empty_v[slot]);
       };
       for (int it = it_begin; it < it_end; ++it) {
         const int4 item = p.items[it];
@@ -482,13 +530,20 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         wait_bar(q_full, q_ph);  // the item's query rows are in tensor memory
         q_ph ^= 1u;
         // the PVs trail the S MMAs by LAG steps, so the in-order tensor pipe always holds
-        // the logits of the next steps ahead of a PV that waits for the softmax
-        constexpr int LAG = T::NSP - 1;
+        // the logits of the next steps ahead of a PV that waits for the softmax (LAG < NSP:
+        // S(g) waits for the PV of step g - NSP, issued before it)
+        constexpr int LAG = T::LAG;
         const uint32_t g_item = g;  // the item's first step
         for (int j = 0; j < nsub; ++j, ++g) {
           const int slot = (int)(g % T::NSTAGE);
-          wait_bar(&full_k[slot], (g / T::NSTAGE) & 1);
-          const uint32_t kbase = smem_addr(smem + T::OFF_K + slot * T::KTILE);
+          uint32_t kbase;
+          if constexpr (T::FP8) {
+            wait_bar(&ck_full[g % T::NCK], (g / T::NCK) & 1);
+            kbase = smem_addr(smem + T::OFF_CV + (g % T::NCK) * T::CV_BUF);
+          } else {
+            wait_bar(&full_k[slot], (g / T::NSTAGE) & 1);
+            kbase = smem_addr(smem + T::OFF_K + slot * T::SLOT);
+          }
           if (g >= (uint32_t)T::NSP) {  // the buffer holds P(g - NSP) until its PV has read it
             const uint32_t x = g - T::NSP;
             wait_bar(&pv_done[x % T::NSP], (x / T::NSP) & 1);
@@ -501,7 +556,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
             umma_f16_ta(t_sg, t_q + kk * 8, bd, ID_S, kk > 0);
           }
           umma_commit(&s_full[g % T::NSP]);
-          umma_commit(&empty_k[slot]);
+          if constexpr (T::FP8)
+            umma_commit(&ck_free[g % T::NCK]);
+          else
+            umma_commit(&empty_k[slot]);
           if (j >= LAG) issue_pv(g - LAG, j == LAG);
         }
         for (int j = nsub > LAG ? nsub - LAG : 0; j < nsub; ++j) issue_pv(g_item + j, j == 0);
@@ -510,13 +568,15 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       umma_commit(mma_end);
       if (!mbar_wait_drain(mma_end, 0)) atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
     }
-  } else {
+  } else if (warp < T::W_CONV) {
     // ================================================================ softmax and epilogue
     const int stid = tid - T::W_SOFT * 32;            // 0 .. 127 over the four warps
     const int r = 32 * (warp & 3) + lane;            // query row = this thread's TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const float qk_scale = p.qk_scale;
-    const float vts = 1.f;
+    const bool tensor_scale = p.scale_mode == PA_SCALE_PER_TENSOR;
+    const float kts = tensor_scale ? __ldg(p.k_scale) : 1.f;
+    const float vts = tensor_scale ? __ldg(p.v_scale) : 1.f;
+    const float qk_scale = p.qk_scale * kts;
     uint32_t g = 0;
     uint32_t pv_next = 0;  // the first step whose PV completion is not consumed yet
     // wait until the PV of step x (which read buffer x % NSP) has completed; completions
@@ -543,6 +603,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       const bool real = r < MP && rg < p.M;
       const int qi = real ? rg / p.G : 0, hq = g_kv * p.G + (real ? rg % p.G : 0);
       const int lim = (real && qi < ql) ? (p.causal ? n - ql + qi + 1 : n) : 0;
+      // a warp whose 32 rows hold no query (the upper half of a 64-row tile) skips the
+      // softmax; its rows of P and O are never read, and it keeps only the waits and
+      // arrivals that keep the barriers' phases in step
+      const bool warp_dead = __all_sync(kFull, !real);
       // ---- this thread's query row into tensor memory, 16-bit pairs (every MMA of the
       // previous item has completed); rows of no query are zero
       {
@@ -553,7 +617,16 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
           uint32_t w[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 v = real ? __ldg(qrow + 8 * h + c) : make_uint4(0, 0, 0, 0);
+            uint4 v = real ? __ldg(qrow + 8 * h + c) : make_uint4(0, 0, 0, 0);
+            if constexpr (T::FP8 && QK == Q_BF16) {  // f16 operands for an fp8 cache
+              uint32_t t4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int jw = 0; jw < 4; ++jw) {
+                const float2 f = bf16x2_to_f2(t4[jw]);
+                t4[jw] = pack16x2<false>(f.x, f.y);
+              }
+              v = make_uint4(t4[0], t4[1], t4[2], t4[3]);
+            }
             w[4 * c] = v.x;
             w[4 * c + 1] = v.y;
             w[4 * c + 2] = v.z;
@@ -571,13 +644,15 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       for (int j = 0; j < nsub; ++j, ++g) {
         const int tok0 = t0 + j * SUB, nv = min(SUB, t1 - tok0);  // tokens of the item here
         if (in_dec && j + 1 == nsub && stid == 0) cnt_seen = ld_acquire_gpu(&p.unit_cnt[u]);
-        if (nv < SUB) {
+        if (!T::FP8 && nv < SUB) {
           // the zeroing below writes into the V slot: the tile must have landed (this wait
           // orders the writes after the copy)
           wait_bar(&full_v[g % T::NSTAGE], (g / T::NSTAGE) & 1);
         }
         wait_bar(&s_full[g % T::NSP], (g / T::NSP) & 1);
         tc_fence_after();
+        if (g >= (uint32_t)T::NSP) wait_pv_step(g - T::NSP);  // (complete: S(g) came after it)
+        if (!warp_dead) {
         const uint32_t t_sg = t_s + (g % T::NSP) * SUB + lane_off;
         float x[SUB];
         tmem_ld64(t_sg, x);
@@ -604,7 +679,6 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         const float mn = need ? mx : m_run;
         const float alpha = (mn == m_run || m_run == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
         m_run = mn;
-        if (g >= (uint32_t)T::NSP) wait_pv_step(g - T::NSP);  // (complete: S(g) came after it)
         // this thread's row of P, 16-bit pairs over the first SUB / 2 columns of its own
         // logits (all of them are in registers); a masked logit (-inf) gives exp2 = 0, and a
         // row with no visible key so far has only zeros
@@ -642,11 +716,12 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
             tmem_st32(t_o + lane_off + 32 * h, o);
           }
         }
+        }  // !warp_dead
         tmem_wait_st();
-        if (nv < SUB) {
+        if (!T::FP8 && nv < SUB) {
           // value rows past the item's tokens may hold anything: zero them (before this
           // step's PV reads them) so that zero weights stay zero
-          char* vt = smem + T::OFF_V + (g % T::NSTAGE) * T::KTILE;
+          char* vt = smem + T::OFF_V + (g % T::NSTAGE) * T::SLOT;
           for (int e = stid; e < (SUB - nv) * T::NSLAB * 8; e += 128) {
             const int rr = nv + e / (T::NSLAB * 8), sl = (e / 8) % T::NSLAB, c = e & 7;
             *reinterpret_cast<uint4*>(vt + sl * T::KSLAB + sw128_chunk(rr, c)) =
@@ -745,13 +820,79 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       pend[2] = pend_odd.x;
       pend[3] = pend_odd.y;
     }
+  } else {
+    // ================================================================ fp8 widening
+    if constexpr (T::FP8) {
+      // step g: the e4m3 K rows of ring slot g % NSTAGE become the f16 rows of K buffer
+      // g % NCK, then its V rows those of V buffer g % NCV (rows past the item's tokens
+      // become zero); the per-tensor scales are applied to the logits and the output
+      const int ctid = tid - T::W_CONV * 32;  // 0 .. 32 NCW - 1
+      // one operand: 64 rows of 128 e4m3 codes -> two slabs of 64 rows of 64 f16 values
+      auto widen = [&](const char* src, char* dst, int nv) {
+#pragma unroll
+        for (int k = 0; k < SUB * 8 / (32 * T::NCW); ++k) {
+          const int e = ctid + k * 32 * T::NCW;
+          const int rr = e / 8, c = e & 7;
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+          if (rr < nv) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + sw128_chunk(rr, c));
+            lo = make_uint4(e4m3x2_to_h2(w.x), e4m3x2_to_h2(w.x >> 16), e4m3x2_to_h2(w.y),
+                            e4m3x2_to_h2(w.y >> 16));
+            hi = make_uint4(e4m3x2_to_h2(w.z), e4m3x2_to_h2(w.z >> 16), e4m3x2_to_h2(w.w),
+                            e4m3x2_to_h2(w.w >> 16));
+          }
+          // dims 16c .. 16c + 15 -> f16 slab c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1
+          char* d = dst + (c >> 2) * T::CV_SLAB;
+          *reinterpret_cast<uint4*>(d + sw128_chunk(rr, 2 * (c & 3))) = lo;
+          *reinterpret_cast<uint4*>(d + sw128_chunk(rr, 2 * (c & 3) + 1)) = hi;
+        }
+        fence_async_smem();
+        __syncwarp();
+      };
+      uint32_t g = 0;
+      for (int it = it_begin; it < it_end; ++it) {
+        const int4 item = p.items[it];
+        const int t0 = item.y, t1 = item.z;
+        if (t1 <= t0) continue;
+        const int nsub = ceil_div(t1 - t0, SUB);
+        for (int j = 0; j < nsub; ++j, ++g) {
+          const int nv = min(SUB, t1 - (t0 + j * SUB));
+          const int slot = (int)(g % T::NSTAGE);
+          const uint32_t ph = (g / T::NSTAGE) & 1;
+          // ---- K rows
+          wait_bar(&full_k[slot], ph);
+          if (g >= (uint32_t)T::NCK) {  // the S of step g - NCK has read this buffer
+            const uint32_t x = g - T::NCK;
+            wait_bar(&ck_free[x % T::NCK], (x / T::NCK) & 1);
+          }
+          widen(smem + T::OFF_K + slot * T::SLOT,
+                smem + T::OFF_CV + (g % T::NCK) * T::CV_BUF, nv);
+          if (lane == 0) {
+            mbar_arrive(&ck_full[g % T::NCK]);
+            mbar_arrive(&empty_k[slot]);  // this warp is done with the K slot
+          }
+          // ---- V rows
+          wait_bar(&full_v[slot], ph);
+          if (g >= (uint32_t)T::NCV) {  // the PV of step g - NCV has read this buffer
+            const uint32_t x = g - T::NCV;
+            wait_bar(&cv_free[x % T::NCV], (x / T::NCV) & 1);
+          }
+          widen(smem + T::OFF_V + slot * T::SLOT,
+                smem + T::OFF_CV + (T::NCK + g % T::NCV) * T::CV_BUF, nv);
+          if (lane == 0) {
+            mbar_arrive(&cv_full[g % T::NCV]);
+            mbar_arrive(&empty_v[slot]);
+          }
+        }
+      }
+    }
   }
 
   tc_fence_before();
   __syncthreads();  // every role is done: no copy or MMA in flight
-  if (warp >= T::W_SOFT) {
+  if (warp >= T::W_SOFT && warp < T::W_CONV) {
     const int stid = tid - T::W_SOFT * 32;
-    finish_pending<D, MP, QK, 4>(p, pend, reinterpret_cast<float*>(smem), T::STAGE / 4, mlbuf, stid);
+    finish_pending<D, MP, QK, 4>(p, pend, reinterpret_cast<float*>(smem), T::SCRATCH / 4, mlbuf, stid);
     zero_empty_units<D, MP, QK, 128>(p, stid);
   }
   __syncthreads();

@@ -84,19 +84,21 @@ constexpr int kTcMinRows = 33;
 
 // Everything but the grid size, which needs the device (see api.cu).
 // Every cache whose tile row is at least one 128-byte slab runs on tensor cores: a 16-bit
-// cache with head dim 128 or 256 and more than 32 query rows per kv head on tcgen05 (row
-// tiles of 64 or 128, the MMA always 128 rows), otherwise on mma.sync with the rows padded to 16, 32
-// or 64 (larger groups cut into 64-row tiles): even a tile of one real row in sixteen costs
-// less there than CUDA-core arithmetic.  (fp8 caches stay on mma.sync, which widens them in
-// registers: the tcgen05 kernel has to widen them in shared memory first, and measured
-// slower.)  A 64-dim fp8 cache (64-byte rows) runs on the CUDA-core kernel, in tiles of up
-// to 8 rows.
+// cache with head dim 128 or 256, or an fp8 cache with head dim 128 and per-tensor or no
+// scales, and more than 32 query rows per kv head on tcgen05 (row tiles of 64 or 128, the
+// MMA always 128 rows), otherwise on mma.sync with the rows padded to 16, 32 or 64 (larger
+// groups cut into 64-row tiles): even a tile of one real row in sixteen costs less there
+// than CUDA-core arithmetic.  (Per-token fp8 scales measured faster on mma.sync, which
+// applies them in registers.)  A 64-dim fp8 cache (64-byte rows) runs on the CUDA-core
+// kernel, in tiles of up to 8 rows.
 inline Variant make_variant(const pa_config& c) {
   Variant v{};
   v.rows = (c.num_q_heads / c.num_kv_heads) * c.max_q_len;
   v.bpe = c.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
   v.path = c.head_dim * v.bpe >= 128 ? 1 : 0;
-  if (v.path == 1 && c.head_dim >= 128 && v.rows >= kTcMinRows && c.kv_dtype != PA_FP8_E4M3)
+  if (v.path == 1 && c.head_dim >= 128 && v.rows >= kTcMinRows &&
+      (c.kv_dtype != PA_FP8_E4M3 ||
+       (c.head_dim == 128 && c.kv_scale_mode != PA_SCALE_PER_TOKEN)))
     v.path = 2;
   if (v.path == 2)
     v.mp = v.rows <= 64 ? 64 : 128;

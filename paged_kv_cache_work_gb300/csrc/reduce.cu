@@ -25,6 +25,8 @@ cudaError_t launch_tc_d128(const KernelParams&, const CUtensorMap&, const CUtens
                            int, int, bool, cudaStream_t);
 cudaError_t launch_tc_d256(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                            int, int, bool, cudaStream_t);
+cudaError_t launch_tc_fp8_d128(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int,
+                               int, int, bool, cudaStream_t);
 
 int mma_ctas_per_sm_d64(int, int, bool);
 int mma_ctas_per_sm_d128(int, int, bool);
@@ -96,6 +98,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CU
   const KernelParams prm = make_kernel_params(a);
   const bool toks = a.scale_mode == PA_SCALE_PER_TOKEN;
   if (a.v.path == 2) {
+    if (a.kv_kind == KV_FP8)
+      return a.p.head_dim == 128
+                 ? launch_tc_fp8_d128(prm, kmap, vmap, a.v.ctas, a.v.mp, a.q_kind, toks, s)
+                 : cudaErrorNotSupported;
     switch (a.p.head_dim) {
       case 128: return launch_tc_d128(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
       case 256: return launch_tc_d256(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);

@@ -145,6 +145,14 @@ EDGE = [
     ("mma_fp8_fp16q_rows32", dict(batch=2, max_q_len=2, num_q_heads=16, num_kv_heads=1,
                                   head_dim=128, block_size=16, ctx=[99, 180], q_dtype="fp16",
                                   kv_dtype="fp8", scale_mode="none")),
+    # per-token fp8 scales stay on mma.sync at every row count
+    ("mma_fp8_token_fp16q_rows64", dict(batch=3, max_q_len=4, num_q_heads=16, num_kv_heads=1,
+                                        head_dim=128, block_size=16, ctx=[129, 70, 640],
+                                        q_dtype="fp16", kv_dtype="fp8", scale_mode="token",
+                                        causal=True)),
+    ("mma_fp8_token_rows100", dict(batch=2, max_q_len=4, num_q_heads=25, num_kv_heads=1,
+                                   head_dim=128, block_size=1024, ctx=[1500, 2049],
+                                   kv_dtype="fp8", scale_mode="token", causal=True)),
     ("mma_d64_fp8_stays_on_cuda_cores", dict(batch=2, max_q_len=1, num_q_heads=16,
                                              num_kv_heads=1, head_dim=64, block_size=16,
                                              ctx=[70, 130], kv_dtype="fp8", scale_mode="token")),
@@ -162,8 +170,9 @@ def test_edge_cases(name, kw, cuda_device, pa):
     assert pa.read_flags(ws) == 0
 
 
-# The tcgen05 kernel: 16-bit caches, head dim 128 or 256, more than 32 query rows per kv head
-# (tiles of 64 or 128 rows, MMA always 128 rows).  The fp8 cases here run on mma.sync.
+# The tcgen05 kernel: 16-bit caches with head dim 128 or 256 and fp8 caches with head dim 128
+# and per-tensor or no scales, more than 32 query rows per kv head (tiles of 64 or 128 rows,
+# MMA always 128 rows).
 TC = [
     ("rows33_padded_causal", dict(batch=3, max_q_len=3, num_q_heads=11, num_kv_heads=1,
                                   block_size=16, ctx=[70, 300, 129], causal=True)),
@@ -178,12 +187,21 @@ TC = [
     ("fp8_tensor_rows64", dict(batch=2, max_q_len=4, num_q_heads=16, num_kv_heads=1,
                                block_size=256, ctx=[260, 1000], kv_dtype="fp8",
                                scale_mode="tensor", causal=True)),
-    ("fp8_token_fp16q_rows64", dict(batch=3, max_q_len=4, num_q_heads=16, num_kv_heads=1,
-                                    block_size=16, ctx=[129, 70, 640], q_dtype="fp16",
-                                    kv_dtype="fp8", scale_mode="token", causal=True)),
+    ("fp8_tensor_fp16q_rows64", dict(batch=3, max_q_len=4, num_q_heads=16, num_kv_heads=1,
+                                     block_size=16, ctx=[129, 70, 640], q_dtype="fp16",
+                                     kv_dtype="fp8", scale_mode="tensor", causal=True)),
     ("fp8_none_rows40_partial", dict(batch=2, max_q_len=5, num_q_heads=8, num_kv_heads=1,
                                      block_size=32, ctx=[5, 191], kv_dtype="fp8",
                                      scale_mode="none", causal=True)),
+    ("fp8_none_rows100_tile128", dict(batch=2, max_q_len=4, num_q_heads=25, num_kv_heads=1,
+                                      block_size=64, ctx=[200, 517], kv_dtype="fp8",
+                                      scale_mode="none", causal=True)),
+    ("fp8_tensor_rows200_two_tiles", dict(batch=2, max_q_len=4, num_q_heads=100,
+                                          num_kv_heads=2, block_size=32, ctx=[333, 64],
+                                          kv_dtype="fp8", scale_mode="tensor", causal=True)),
+    ("fp8_tensor_long_pages", dict(batch=2, max_q_len=4, num_q_heads=16, num_kv_heads=1,
+                                   block_size=1024, ctx=[1500, 2049], kv_dtype="fp8",
+                                   scale_mode="tensor", causal=True)),
     ("ragged_and_empty", dict(batch=4, max_q_len=4, num_q_heads=16, num_kv_heads=1,
                               block_size=16, ctx=[0, 4, 63, 65], q_lens=[0, 4, 1, 3],
                               causal=True)),
