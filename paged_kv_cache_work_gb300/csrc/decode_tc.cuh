@@ -11,9 +11,10 @@
 //               (M = 128, N = head dim, K = 64, V read as an MN-major operand), so the
 //               in-order tensor pipe holds the next logits ahead of any PV that waits for
 //               the softmax;
-//   warps 6-7   (fp8 caches, per-tensor or no scales) widen each step's e4m3 K rows to
+//   warps 6-9   (fp8 caches, per-tensor or no scales) widen each step's e4m3 K rows to
 //               f16 in one of three shared-memory buffers, released by the step's S, and
-//               its V rows in one of four, released by its PV;
+//               its V rows in one of four, released by its PV (one warp per SM
+//               sub-partition: the conversion rate, not the copy, bounds fewer warps);
 //   warps 2-5   one query row per thread: load the row's logits with tcgen05.ld, online
 //               softmax in registers (a row never leaves its thread), write the row of P as
 //               16-bit pairs over the first half of the same logits buffer; at the end of an
@@ -43,7 +44,7 @@ struct TcTraits {
   static constexpr bool FP8 = KVK == KV_FP8;
   static constexpr int BPE = FP8 ? 1 : 2;
   static constexpr int W_PROD = 0, W_MMA = 1, W_SOFT = 2, W_CONV = 6;
-  static constexpr int NCW = FP8 ? 2 : 0;  // warps that widen fp8 tiles to f16
+  static constexpr int NCW = FP8 ? 4 : 0;  // warps that widen fp8 tiles to f16
   static constexpr int NW = 6 + NCW;
   static constexpr int NTHREADS = NW * 32;
   static constexpr int TT = kTcStepTokens;  // tokens per tile and per MMA step: 64
