@@ -12,7 +12,9 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 CASES = [W.reduced(W.GQA_B32, 8, 300, 3000), W.reduced(W.LONG_SQ4, 2, 20000, 40000),
-         W.reduced(W.FP8_TOKEN_SQ4, 4, 2000, 5000), W.reduced(W.mha_d256(8, 4), 4, 500, 3000)]
+         W.reduced(W.FP8_TOKEN_SQ4, 4, 2000, 5000), W.reduced(W.mha_d256(8, 4), 4, 500, 3000),
+         # the tcgen05 kernel at head dim 256 and with an fp8 cache
+         W.reduced(W.mha_d256(8, 64), 3, 500, 3000), W.reduced(W.FP8_TENSOR_SQ4, 4, 2000, 5000)]
 
 
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
