@@ -1,5 +1,6 @@
 // Fifth-generation tensor-core decode (tcgen05, accumulators in tensor memory) for large
-// query tiles: 33 to 128 query rows per kv head, head dim 128 or 256, 16-bit caches.
+// query tiles: 33 to 128 query rows per kv head, 16-bit caches of head dim 128 or 256 and
+// fp8 caches of head dim 128 with per-tensor or no scales.
 //
 // A step is a tile of 64 tokens.  The CTA is split into roles that talk only through
 // mbarriers, so copies, MMAs and the softmax of different steps overlap:
@@ -11,19 +12,20 @@
 //               (M = 128, N = head dim, K = 64, V read as an MN-major operand), so the
 //               in-order tensor pipe holds the next logits ahead of any PV that waits for
 //               the softmax;
-//   warps 6-9   (fp8 caches, per-tensor or no scales) widen each step's e4m3 K rows to
-//               f16 in one of three shared-memory buffers, released by the step's S, and
-//               its V rows in one of four, released by its PV (one warp per SM
-//               sub-partition: the conversion rate, not the copy, bounds fewer warps);
 //   warps 2-5   one query row per thread: load the row's logits with tcgen05.ld, online
 //               softmax in registers (a row never leaves its thread), write the row of P as
 //               16-bit pairs over the first half of the same logits buffer; at the end of an
 //               item load O from tensor memory and write the output or the split partial
-//               (merge protocol of decode_common.cuh).
+//               (merge protocol of decode_common.cuh);
+//   warps 6-9   (fp8 caches) widen each step's e4m3 K rows to f16 in one of three
+//               shared-memory buffers, released by the step's S, and its V rows in one of
+//               four, released by its PV (one warp per SM sub-partition: with fewer, the
+//               conversion rate, not the copy, bounds the kernel).
 // Buffer g % NSP holds S(g) and then P(g) until the PV of step g has read it, so the MMA
 // thread waits for that PV before it writes S(g + NSP) there: NSP = 4 at head dim 128 and
 // 2 at head dim 256, as many as tensor memory holds next to O and the query rows (Q, as
-// 16-bit pairs: lane = row).  Shared memory carries only K and V.
+// 16-bit pairs: lane = row).  Shared memory carries only K and V (and, for fp8, their f16
+// widening).
 //
 // A tcgen05.mma of K = 16 occupies the tensor pipe about equally long at every N up to
 // 256, so these N = 64 logits use a quarter of its peak: at head dim 256 (16 S MMAs and 4
@@ -263,8 +265,9 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 // The TMA side of the tcgen05 kernel, run by warp 0 (all lanes, same state).  Tile n of the
 // CTA's work list goes to slot n % NSTAGE of the K ring and of the V ring; lane
 // page * NSLAB + slab copies one 128-byte column slab of one page of the tile.  The order of
-// the copies is K(0), K(1), V(0), K(2), V(1), ...: a K copy waits for the S of the tile
-// NSTAGE earlier, a V copy for its PV.
+// the copies is K(0), K(1), V(0), K(2), V(1), ...: a copy waits until the tile NSTAGE
+// earlier has been read from its slot (by its S for K and its PV for V, or, for fp8, by the
+// widening warps).
 template <class T>
 struct TcProducer {
   struct Box {
@@ -494,8 +497,8 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       uint32_t q_ph = 0, o_ph = 0;
       // step x uses buffer x % NSP; every barrier of a buffer completes once per use, in
       // step order, so the phase of step x is (x / NSP) & 1
-      // O += P V of step gp (its P, in buffer gp % 2, must be written); the commit releases
-      // the V slot
+      // O += P V of step gp (its P, in buffer gp % NSP, must be written); the commit releases
+      // the V slot (fp8: the V buffer)
       auto issue_pv = [&](uint32_t gp, bool first) {
         const int slot = (int)(gp % T::NSTAGE);
         uint32_t vaddr;
@@ -654,69 +657,69 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         tc_fence_after();
         if (g >= (uint32_t)T::NSP) wait_pv_step(g - T::NSP);  // (complete: S(g) came after it)
         if (!warp_dead) {
-        const uint32_t t_sg = t_s + (g % T::NSP) * SUB + lane_off;
-        float x[SUB];
-        tmem_ld64(t_sg, x);
-        // ---- online softmax of this thread's row (log2 units), two logits per instruction
-        const float2 s2 = make_float2(qk_scale, qk_scale), z2 = make_float2(0.f, 0.f);
+          const uint32_t t_sg = t_s + (g % T::NSP) * SUB + lane_off;
+          float x[SUB];
+          tmem_ld64(t_sg, x);
+          // ---- online softmax of this thread's row (log2 units), two logits per instruction
+          const float2 s2 = make_float2(qk_scale, qk_scale), z2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < SUB / 2; ++i) {
-          const float2 y = ffma2(make_float2(x[2 * i], x[2 * i + 1]), s2, z2);
-          x[2 * i] = y.x;
-          x[2 * i + 1] = y.y;
-        }
-        // masked keys (past the item's tokens or past the row's causal limit) become -inf;
-        // most steps have none
-        if (nv < SUB || tok0 + SUB > lim) {
+          for (int i = 0; i < SUB / 2; ++i) {
+            const float2 y = ffma2(make_float2(x[2 * i], x[2 * i + 1]), s2, z2);
+            x[2 * i] = y.x;
+            x[2 * i + 1] = y.y;
+          }
+          // masked keys (past the item's tokens or past the row's causal limit) become -inf;
+          // most steps have none
+          if (nv < SUB || tok0 + SUB > lim) {
 #pragma unroll
-          for (int jj = 0; jj < SUB; ++jj)
-            if (jj >= nv || tok0 + jj >= lim) x[jj] = -INFINITY;
-        }
-        float mx = -INFINITY;
+            for (int jj = 0; jj < SUB; ++jj)
+              if (jj >= nv || tok0 + jj >= lim) x[jj] = -INFINITY;
+          }
+          float mx = -INFINITY;
 #pragma unroll
-        for (int jj = 0; jj < SUB; jj += 2) mx = fmaxf(mx, fmaxf(x[jj], x[jj + 1]));
-        const bool need = mx > m_run + 8.f;  // lazy rescale: only when the max grows by 2^8
-        const bool rescale = __any_sync(kFull, need);
-        const float mn = need ? mx : m_run;
-        const float alpha = (mn == m_run || m_run == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
-        m_run = mn;
-        // this thread's row of P, 16-bit pairs over the first SUB / 2 columns of its own
-        // logits (all of them are in registers); a masked logit (-inf) gives exp2 = 0, and a
-        // row with no visible key so far has only zeros
-        float lsum = 0.f;
-        {
-          const float2 nm = make_float2(m_run == -INFINITY ? 0.f : -m_run,
-                                        m_run == -INFINITY ? 0.f : -m_run);
-          const float2 one2 = make_float2(1.f, 1.f);
-          float2 ls2 = z2;
+          for (int jj = 0; jj < SUB; jj += 2) mx = fmaxf(mx, fmaxf(x[jj], x[jj + 1]));
+          const bool need = mx > m_run + 8.f;  // lazy rescale: only when the max grows by 2^8
+          const bool rescale = __any_sync(kFull, need);
+          const float mn = need ? mx : m_run;
+          const float alpha = (mn == m_run || m_run == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
+          m_run = mn;
+          // this thread's row of P, 16-bit pairs over the first SUB / 2 columns of its own
+          // logits (all of them are in registers); a masked logit (-inf) gives exp2 = 0, and a
+          // row with no visible key so far has only zeros
+          float lsum = 0.f;
+          {
+            const float2 nm = make_float2(m_run == -INFINITY ? 0.f : -m_run,
+                                          m_run == -INFINITY ? 0.f : -m_run);
+            const float2 one2 = make_float2(1.f, 1.f);
+            float2 ls2 = z2;
 #pragma unroll
-          for (int h = 0; h < SUB / 32; ++h) {  // 32 tokens = 16 columns at a time
-            uint32_t pk[16];
+            for (int h = 0; h < SUB / 32; ++h) {  // 32 tokens = 16 columns at a time
+              uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 t = ffma2(make_float2(x[32 * h + 2 * i], x[32 * h + 2 * i + 1]), one2, nm);
-              const float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
-              ls2 = ffma2(make_float2(p0, p1), one2, ls2);
-              pk[i] = pack16x2<BF>(p0, p1);
+              for (int i = 0; i < 16; ++i) {
+                const float2 t = ffma2(make_float2(x[32 * h + 2 * i], x[32 * h + 2 * i + 1]), one2, nm);
+                const float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
+                ls2 = ffma2(make_float2(p0, p1), one2, ls2);
+                pk[i] = pack16x2<BF>(p0, p1);
+              }
+              tmem_st16u(t_sg + 16 * h, pk);
             }
-            tmem_st16u(t_sg + 16 * h, pk);
+            lsum = ls2.x + ls2.y;
           }
-          lsum = ls2.x + ls2.y;
-        }
-        l_run = l_run * alpha + lsum;
-        if (rescale && j > 0) {
-          // O holds earlier tokens of this item: scale this warp's rows once every PV into
-          // O has completed (the PV of this step waits for p_full below)
-          wait_pv_step(g - 1);
+          l_run = l_run * alpha + lsum;
+          if (rescale && j > 0) {
+            // O holds earlier tokens of this item: scale this warp's rows once every PV into
+            // O has completed (the PV of this step waits for p_full below)
+            wait_pv_step(g - 1);
 #pragma unroll 1
-          for (int h = 0; h < D / 32; ++h) {
-            float o[32];
-            tmem_ld32(t_o + lane_off + 32 * h, o);
+            for (int h = 0; h < D / 32; ++h) {
+              float o[32];
+              tmem_ld32(t_o + lane_off + 32 * h, o);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) o[jj] *= alpha;
-            tmem_st32(t_o + lane_off + 32 * h, o);
+              for (int jj = 0; jj < 32; ++jj) o[jj] *= alpha;
+              tmem_st32(t_o + lane_off + 32 * h, o);
+            }
           }
-        }
         }  // !warp_dead
         tmem_wait_st();
         if (!T::FP8 && nv < SUB) {
