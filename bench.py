@@ -398,6 +398,7 @@ def run_ours(args, rank, world, local):
                 "l2": (f"inputs larger than L2: 2 input sets of {int(bytes_per_launch) >> 20} MiB KV "
                        f"alternate (L2 {l2 >> 20} MiB)"),
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                "grid_mult": int(cfg.grid_mult) or 1,
                 "split_merge": "auto (decode's last CTA merges units of few pieces, "
                                "the reduce kernel the rest)",
             },

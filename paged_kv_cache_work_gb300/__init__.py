@@ -161,16 +161,25 @@ _SM = {"none": SCALE_NONE, "tensor": SCALE_PER_TENSOR, "token": SCALE_PER_TOKEN}
 
 def config_for(inp: dict, num_ctas: int = 0, grid_mult: int = 0,
                split_merge: int = MERGE_AUTO) -> PaConfig:
-    """pa_config of a problem laid out as workloads.make_inputs returns it."""
+    """pa_config of a problem laid out as workloads.make_inputs returns it.  With neither a
+    grid size nor a multiplier given and the inputs on a GPU, the multiplier comes from the
+    tuned table (grid_tune.lookup: 1 for shapes it does not list)."""
     w = inp["workload"]
-    return PaConfig(batch=w.batch, max_q_len=w.max_q_len, num_q_heads=w.num_q_heads,
-                    num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, block_size=w.block_size,
-                    max_blocks_per_seq=inp["block_tables"].shape[1],
-                    num_blocks=inp["k_cache"].shape[0], q_dtype=_DT[w.q_dtype],
-                    kv_dtype=_DT[w.kv_dtype],
-                    kv_scale_mode=_SM[w.scale_mode] if w.kv_dtype == "fp8" else SCALE_NONE,
-                    causal=int(w.causal), sm_scale=float(inp["sm_scale"]), num_ctas=num_ctas,
-                    grid_mult=grid_mult, split_merge=split_merge)
+    cfg = PaConfig(batch=w.batch, max_q_len=w.max_q_len, num_q_heads=w.num_q_heads,
+                   num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, block_size=w.block_size,
+                   max_blocks_per_seq=inp["block_tables"].shape[1],
+                   num_blocks=inp["k_cache"].shape[0], q_dtype=_DT[w.q_dtype],
+                   kv_dtype=_DT[w.kv_dtype],
+                   kv_scale_mode=_SM[w.scale_mode] if w.kv_dtype == "fp8" else SCALE_NONE,
+                   causal=int(w.causal), sm_scale=float(inp["sm_scale"]), num_ctas=num_ctas,
+                   grid_mult=grid_mult, split_merge=split_merge)
+    q = inp["q"]
+    if num_ctas == 0 and grid_mult == 0 and getattr(q, "is_cuda", False):
+        import torch
+        from . import grid_tune
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        cfg.grid_mult = grid_tune.lookup(cfg, sms)
+    return cfg
 
 
 def paged_attention(inp: dict, out=None, lse=None, ws=None, cfg: Optional[PaConfig] = None,

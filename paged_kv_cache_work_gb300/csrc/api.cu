@@ -49,7 +49,8 @@ pa_status validate(const pa_config* c) {
 }
 
 // Persistent grid: num_ctas if given, else (SMs x grid_mult) x the decode CTAs that fit
-// on one SM, so the whole grid is resident at once.
+// on one SM: one resident wave at multiplier 1; with a larger one the later CTAs start as
+// earlier ones finish.
 pa_status resolve_ctas(const pa_config& c, Variant* v) {
   if (c.num_ctas > 0) {
     v->ctas = c.num_ctas > 65535 ? 65535 : c.num_ctas;

@@ -310,3 +310,19 @@ def test_empty_sequences_with_reduce_kernel(cuda_device, pa):
     ref_out, ref_lse = oracle.decode(inp, "f32")
     out, lse, _, _ = run(W.to_device(inp, cuda_device), num_ctas=7, split_merge=pa.MERGE_IN_REDUCE)
     compare(out, lse, ref_out, ref_lse, "bf16")
+
+# Grid multipliers above 1 (more CTAs than one wave; the later ones start as earlier ones
+# finish): every kernel family, compared with the oracle.
+GRID_CASES = [W.reduced(W.GQA_B32, 6, 300, 2000), W.reduced(W.LONG_SQ4, 2, 3000, 9000),
+              W.reduced(W.FP8_TENSOR_SQ4, 3, 1000, 4000), W.reduced(W.mha_d256(4, 64), 2, 300, 1500)]
+
+
+@pytest.mark.parametrize("mult", [2, 4])
+@pytest.mark.parametrize("wl", GRID_CASES, ids=lambda w: w.name)
+def test_grid_multiplier(wl, mult, cuda_device, pa):
+    inp = W.make_inputs(wl, W.SEEDS[1])
+    ref_out, ref_lse = oracle.decode(inp, "f32")
+    out, lse, ws, cfg = run(W.to_device(inp, cuda_device), grid_mult=mult)
+    assert cfg.grid_mult == mult
+    compare(out, lse, ref_out, ref_lse, wl.kv_dtype)
+    assert pa.read_flags(ws) == 0
