@@ -20,7 +20,8 @@ L2: two independent input sets of > 2x L2 bytes each alternate between steps, so
 step finds its KV in L2.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload NAME] [--all] [--no-cpu-baseline]
+                       [--workload NAME] [--all] [--no-cpu-baseline] [--gather]
+--gather times the paged -> contiguous KV copy (pa_gather_kv) of the workload instead.
 For N > 1 launch with torchrun (one process per GPU).
 """
 from __future__ import annotations
@@ -462,6 +463,63 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_gather(args, local):
+    """The paged -> contiguous copy (pa_gather_kv) of one workload's whole cache: bytes read
+    plus bytes written per call over the device time of K calls (two input sets alternate,
+    each larger than L2), against the measured HBM copy peak."""
+    import torch
+    import paged_kv_cache_work_gb300 as pa
+    import workloads as W
+    dev = torch.device("cuda", local)
+    wl = W.FULL[args.workload]
+    pa.load()
+    sets = [W.make_inputs(wl, W.SEEDS[0] + 7919 * k, device=dev) for k in range(2)]
+    row_elems = wl.num_kv_heads * wl.head_dim
+    bufs = []
+    for s in sets:
+        rows = int(s["context_lens"].sum().item())
+        cfg = pa.config_for(s, num_ctas=1)
+        k_out = torch.empty((rows, wl.num_kv_heads, wl.head_dim), dtype=s["k_cache"].dtype,
+                            device=dev)
+        bufs.append((s, cfg, k_out, torch.empty_like(k_out), rows,
+                     torch.zeros(1, dtype=torch.int32, device=dev)))
+    bytes_per = [2 * 2 * rows * row_elems * s["k_cache"].element_size()
+                 for s, _, _, _, rows, _ in bufs]  # K and V, read and written
+    stream = torch.cuda.current_stream(dev)
+
+    def call(i):
+        s, cfg, k_out, v_out, rows, flags = bufs[i % 2]
+        pa.gather_kv(cfg, s["k_cache"], s["v_cache"], s["block_tables"], s["context_lens"],
+                     k_out, v_out, rows, None, flags, stream.cuda_stream)
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    for b in bufs:
+        if int(b[5].item()):
+            raise RuntimeError(f"device flags {int(b[5].item())} in the gather")
+    sec = e0.elapsed_time(e1) / 1e3
+    total = sum(bytes_per[i % 2] for i in range(args.steps))
+    gbs = total / sec / 1e9
+    peak, src = measured_hbm_peak()
+    return {"metric": "paged->contiguous KV gather GB/s (bytes read + written)",
+            "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "us_per_call": round(sec / args.steps * 1e6, 2),
+            "higher_is_better": True, "dtype": wl.kv_dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "kv_bytes_read_per_call": int(statistics.fmean(bytes_per) / 2),
+                       "l2": "inputs larger than L2: 2 input sets alternate"},
+            "roofline": {"kernel": "gather_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                         "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
+                         if src == "measured" else src}}
+
+
 def main(argv=None):
     import workloads as W
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
@@ -472,6 +530,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=W.BENCH.name, choices=sorted(W.FULL))
     ap.add_argument("--all", action="store_true", help="one line per workload family")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gather", action="store_true",
+                    help="time the paged -> contiguous copy (pa_gather_kv) of the workload instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -480,6 +540,10 @@ def main(argv=None):
         res = run_reference(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return 0
+    if args.gather:
+        if rank == 0:
+            print(json.dumps(run_gather(args, local)), flush=True)
         return 0
     if world > 1:
         import torch.distributed as dist

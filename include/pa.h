@@ -189,6 +189,38 @@ PA_API pa_status pa_decode_step_static(const pa_config *cfg, const void *q, cons
                                        const int32_t *context_lens, const int32_t *q_lens,
                                        void *out, float *lse, pa_stream stream);
 
+/* Paged -> contiguous copy of a batch's cached K and V (the copy the HSTU paged attention
+ * makes from its paged cache into its workspace before attending: "HSTU Paged Attention"
+ * K/V double-buffering issue, background and optimisation plan).
+ *
+ * Sequence b's tokens 0 .. context_lens[b] - 1 are copied, in token order, to rows
+ * row_off[b] .. row_off[b] + context_lens[b] - 1 of k_out and of v_out, where
+ * row_off[b] = context_lens[0] + ... + context_lens[b - 1]; a row is one token's
+ * [num_kv_heads, head_dim] values exactly as the cache stores them (bf16, fp16 or E4M3
+ * codes; per-token fp8 scales are not copied).  Reads cfg's batch, num_kv_heads, head_dim,
+ * block_size, max_blocks_per_seq, num_blocks and kv_dtype; the other fields are ignored.
+ *
+ *   k_cache, v_cache  device, [num_blocks, block_size, num_kv_heads, head_dim], 16-byte aligned
+ *   block_tables      device int32 [batch, max_blocks_per_seq]
+ *   context_lens      device int32 [batch]
+ *   k_out, v_out      device, room for max_rows rows of num_kv_heads * head_dim elements,
+ *                     16-byte aligned
+ *   row_offsets       NULL, or device int32 [batch + 1] that receives row_off[0 .. batch]
+ *                     (row_off[batch] = rows copied)
+ *   flags             NULL, or a device int32 the call ORs PA_FLAG_* bits into:
+ *                     PA_FLAG_BAD_LENGTHS when a length is negative or exceeds
+ *                     max_blocks_per_seq * block_size (that sequence counts as empty) or the
+ *                     rows exceed max_rows (nothing is copied), PA_FLAG_BAD_BLOCK_ID for a
+ *                     page whose block id lies outside [0, num_blocks) (its rows are not
+ *                     written)
+ *
+ * Stream-ordered, allocates nothing.  PA_ERR_UNSUPPORTED for batch > 8192, head_dim or
+ * block_size outside the decode's sets, or problems whose row or copy counts exceed int32. */
+PA_API pa_status pa_gather_kv(const pa_config *cfg, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, const int32_t *context_lens,
+                              void *k_out, void *v_out, int64_t max_rows, int32_t *row_offsets,
+                              int32_t *flags, pa_stream stream);
+
 /* A static, human-readable name of a status. */
 PA_API const char *pa_status_string(pa_status status);
 

@@ -225,3 +225,30 @@ def threads() -> int:
 
 __all__ = ["decode", "decode_rows", "attend_range", "merge", "e4m3", "bf16", "fp16", "lib",
            "libs_from", "threads"]
+
+
+def gather_kv(inp: dict):
+    """Paged -> contiguous copy of every cached token's K and V rows (the copy from the paged
+    KV cache into the attention's workspace, "HSTU Paged Attention" K/V double-buffering
+    issue, background section), written out from its definition: sequence b's token j,
+    0 <= j < context_lens[b], is row j % block_size of block block_tables[b][j // block_size],
+    and the sequences follow one another in batch order.
+
+    Returns (k_rows, v_rows, row_offsets): the rows as the cache stores them (numpy arrays of
+    the cache's element bits, [total_tokens, Hkv, D]) and the int64 offsets [B + 1]."""
+    w = inp["workload"]
+    bs = w.block_size
+    bt = inp["block_tables"].cpu().numpy()
+    ctx = inp["context_lens"].cpu().numpy().astype(np.int64)
+    out = []
+    for name in ("k_cache", "v_cache"):
+        cache = inp[name].detach().cpu().contiguous()
+        bits = cache.view(torch.uint8) if cache.element_size() == 1 else cache.view(torch.int16)
+        cache_np = bits.numpy()
+        parts = []
+        for b in range(len(ctx)):
+            j = np.arange(ctx[b])
+            parts.append(cache_np[bt[b][j // bs], j % bs])
+        out.append(np.concatenate(parts, axis=0) if parts else cache_np[:0, 0])
+    offsets = np.concatenate([[0], np.cumsum(ctx)])
+    return out[0], out[1], offsets

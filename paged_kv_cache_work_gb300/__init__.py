@@ -33,7 +33,7 @@ FLAG_BAD_LENGTHS, FLAG_BAD_BLOCK_ID, FLAG_WAIT_TIMEOUT = 1, 2, 4
 MERGE_AUTO, MERGE_IN_DECODE, MERGE_IN_REDUCE = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("pa_workspace_size", "pa_plan", "pa_decode", "pa_reduce", "pa_read_flags",
-                    "pa_status_string", "pa_decode_step_static")
+                    "pa_status_string", "pa_decode_step_static", "pa_gather_kv")
 
 # Bytes of the device array behind pa_decode_step_static (PA_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -76,6 +76,8 @@ def load(path: str = LIB_PATH):
         getattr(L, f).restype = ctypes.c_int
     L.pa_decode_step_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.pa_decode_step_static.restype = ctypes.c_int
+    L.pa_gather_kv.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp]
+    L.pa_gather_kv.restype = ctypes.c_int
     L.pa_status_string.argtypes = [ctypes.c_int]
     L.pa_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -152,6 +154,16 @@ def decode_step_static(cfg: PaConfig, q, k_cache, v_cache, k_scale, v_scale, blo
     _check("pa_decode_step_static", load().pa_decode_step_static(
         ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
         _ptr(block_tables), _ptr(context_lens), _ptr(q_lens), _ptr(out), _ptr(lse),
+        _stream(stream)))
+
+
+def gather_kv(cfg: PaConfig, k_cache, v_cache, block_tables, context_lens, k_out, v_out,
+              max_rows: int, row_offsets=None, flags=None, stream=None):
+    """Paged -> contiguous copy of the batch's K and V rows (see pa_gather_kv in pa.h):
+    sequence b lands at rows row_offsets[b] .. row_offsets[b + 1] - 1 of k_out and v_out."""
+    _check("pa_gather_kv", load().pa_gather_kv(
+        ctypes.byref(cfg), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(k_out), _ptr(v_out), int(max_rows), _ptr(row_offsets), _ptr(flags),
         _stream(stream)))
 
 

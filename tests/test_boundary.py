@@ -133,6 +133,25 @@ def test_null_arguments_rejected_before_any_launch(lib):
     assert lib.pa_read_flags(fake, 1024, None, None) == pa.ERR_INVALID_ARG
 
 
+def test_gather_arguments_rejected_before_any_launch(lib):
+    fake = 1 << 20  # never dereferenced: every call below is rejected on the host
+    g = lambda c, kc=fake, vc=fake, bt=fake, cl=fake, ko=fake, vo=fake, rows=1000: \
+        lib.pa_gather_kv(ctypes.byref(c), kc, vc, bt, cl, ko, vo, rows, None, None, None)
+    cfg = base_cfg()
+    assert lib.pa_gather_kv(None, fake, fake, fake, fake, fake, fake, 10, None, None,
+                            None) == pa.ERR_INVALID_ARG
+    for kw in (dict(kc=None), dict(vc=None), dict(bt=None), dict(cl=None), dict(ko=None),
+               dict(vo=None)):
+        assert g(cfg, **kw) == pa.ERR_INVALID_ARG, kw
+    assert g(cfg, kc=fake + 8) == pa.ERR_INVALID_ARG   # cache not 16-byte aligned
+    assert g(cfg, vo=fake + 4) == pa.ERR_INVALID_ARG   # output not aligned
+    assert g(cfg, rows=-1) == pa.ERR_INVALID_ARG
+    assert g(base_cfg(head_dim=96)) == pa.ERR_UNSUPPORTED
+    assert g(base_cfg(block_size=24)) == pa.ERR_UNSUPPORTED
+    assert g(base_cfg(batch=8193)) == pa.ERR_UNSUPPORTED
+    assert g(base_cfg(batch=0)) == pa.ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     seen = set()
     for s in range(6):
