@@ -41,6 +41,10 @@
  * Device pointers: q, k_cache, v_cache, k_scale, v_scale, block_tables,
  * context_lens, q_lens, out, lse and ws.  q, k_cache, v_cache and out must be
  * 16-byte aligned; ws 256-byte aligned.
+ *
+ * Besides the step, pa_gather_kv copies a batch's cached K and V rows out of the
+ * pages into contiguous buffers (the workspace copy of the HSTU paged attention),
+ * with the same calling convention.
  */
 #ifndef PA_H_
 #define PA_H_
