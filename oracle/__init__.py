@@ -82,6 +82,10 @@ def lib(precision: str = "f32"):
             getattr(L, name).restype = real
         L.oracle_e4m3.argtypes = [ctypes.c_uint8]
         L.oracle_e4m3.restype = real
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_append_kv.argtypes = [cp, vp, vp, i32p, i32p, i32p, vp, vp, fp, fp]
+        L.oracle_append_kv.restype = ctypes.c_int
         assert L.oracle_real_bytes() == (4 if precision == "f32" else 8)
         _libs[precision] = (L, real)
     return _libs[precision]
@@ -204,6 +208,12 @@ def e4m3(code: int, precision: str = "f64") -> float:
     return float(lib(precision)[0].oracle_e4m3(code))
 
 
+def e4m3_encode(x: float, precision: str = "f64") -> int:
+    """OCP E4M3 code of the float32 value x: clamped to +-448, nearest grid point, ties to
+    the even code (the encoding step of the quantise-on-write append)."""
+    return int(lib(precision)[0].oracle_e4m3_encode(float(np.float32(x))))
+
+
 def bf16(bits: int, precision: str = "f64") -> float:
     return float(lib(precision)[0].oracle_bf16(bits))
 
@@ -223,8 +233,8 @@ def threads() -> int:
         return os.cpu_count() or 1
 
 
-__all__ = ["decode", "decode_rows", "attend_range", "merge", "e4m3", "bf16", "fp16", "lib",
-           "libs_from", "threads"]
+__all__ = ["decode", "decode_rows", "attend_range", "merge", "e4m3", "e4m3_encode", "bf16",
+           "fp16", "lib", "libs_from", "threads", "gather_kv", "append_kv"]
 
 
 def gather_kv(inp: dict):
@@ -252,3 +262,38 @@ def gather_kv(inp: dict):
         out.append(np.concatenate(parts, axis=0) if parts else cache_np[:0, 0])
     offsets = np.concatenate([[0], np.cumsum(ctx)])
     return out[0], out[1], offsets
+
+
+def append_kv(inp: dict, k_new: torch.Tensor, v_new: torch.Tensor, precision: str = "f64"):
+    """Quantise-on-write KV append, written out from its definition in pa_oracle.c: new row
+    i < q_lens[b] of sequence b (k_new / v_new [B, Sq, Hkv, D] in the query dtype) goes to
+    position context_lens[b] - q_lens[b] + i of that sequence, i.e. slot pos % block_size of
+    block block_tables[b][pos // block_size]; an fp8 cache receives E4M3 codes of the row over
+    its scale (per-token scales amax/448 are written too; a per-tensor scale is read).
+
+    ``inp`` holds the cache as workloads.make_inputs lays it out.  Returns new host tensors
+    (k_cache, v_cache, k_scale, v_scale); the inputs are not modified."""
+    L, _ = lib(precision)
+    w = inp["workload"]
+    cfg = _Prepared(inp).cfg
+    kc = _host(inp["k_cache"]).clone()
+    vc = _host(inp["v_cache"]).clone()
+    ks = _host(inp.get("k_scale"))
+    vs = _host(inp.get("v_scale"))
+    ks = None if ks is None else ks.float().clone()
+    vs = None if vs is None else vs.float().clone()
+    kn = _host(k_new)
+    vn = _host(v_new)
+    qdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[w.q_dtype]
+    assert kn.dtype == qdt and vn.dtype == qdt, "new rows are in the query dtype"
+    assert tuple(kn.shape) == (w.batch, w.max_q_len, w.num_kv_heads, w.head_dim)
+    bt = _host(inp["block_tables"]).to(torch.int32)
+    ctx = _host(inp["context_lens"]).to(torch.int32)
+    ql = _host(inp["q_lens"]).to(torch.int32)
+    i32 = ctypes.c_int32
+    f = ctypes.c_float
+    rc = L.oracle_append_kv(ctypes.byref(cfg), _ptr(kn), _ptr(vn), _ptr(bt, i32), _ptr(ctx, i32),
+                            _ptr(ql, i32), _ptr(kc), _ptr(vc), _ptr(ks, f), _ptr(vs, f))
+    if rc != 0:
+        raise ValueError(f"oracle_append_kv rejected the problem (code {rc})")
+    return kc, vc, ks, vs

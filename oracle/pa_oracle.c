@@ -289,3 +289,118 @@ int oracle_attend_range(const oracle_cfg *c, const void *q, const void *k, const
   if (j0 > j1) j0 = j1;
   return attend_range(&p, b, i, h, j0, j1, o, lse);
 }
+
+/* ------------------------------------------------------------------------------------
+ * KV append with quantise-on-write: the step that fills the paged cache the decode reads.
+ *
+ * A decode step's q_len new tokens of sequence b are the last q_len positions of its
+ * context_len cached tokens (the convention of the decode above), so new row i of
+ * sequence b is stored at position pos = context_len - q_len + i, which is slot pos % bs
+ * of physical block block_tables[b][pos / bs] ("HSTU Paged Attention", RecSDK issue 1281,
+ * background: K/V live in a paged cache read through per-sequence page lists).  A 16-bit
+ * cache receives the new row's bits unchanged.  An fp8 cache receives E4M3 codes of the
+ * row divided by its scale, one of the scale modes of "Optimize paged-attention metadata
+ * decode" (FlyDSL PR #910, Breaking Changes: per_token_kv): per-token, the scale of the
+ * (block, slot, kv-head) row is its largest magnitude over 448 (the E4M3 maximum), or 1
+ * for an all-zero row, and is written next to the codes; per-tensor, the one scale the
+ * caller holds is used as it is; with no scale the values are encoded directly.
+ *
+ * The scale and the quotient are float (binary32) operations, as the scales are stored
+ * in float; the code is the E4M3 value nearest to the quotient clamped to [-448, 448],
+ * ties to the even code.  These are float in both builds of this file, so a code is the
+ * same integer decision whatever `real` is.
+ * ------------------------------------------------------------------------------------ */
+
+/* Round-half-to-even of t >= 0 to an integer (kept in a double). */
+static double round_half_even(double t) {
+  double fl = floor(t), fr = t - fl;
+  if (fr > 0.5 || (fr == 0.5 && fmod(fl, 2.0) == 1.0)) fl += 1.0;
+  return fl;
+}
+
+/* OCP E4M3 code of x: magnitude clamped to 448, rounded to the nearest point of the E4M3
+ * grid (ties to even), NaN to 0x7f.  In the binade [2^e, 2^(e+1)), e >= -6, the grid
+ * spacing is 2^(e-3); below 2^-6 (subnormals) it is 2^-9. */
+uint8_t oracle_e4m3_encode(float x) {
+  if (isnan(x)) return 0x7f;
+  int sign = signbit(x) ? 1 : 0;
+  double a = fabs((double)x);
+  if (a > 448.0) a = 448.0;
+  int e = -6;
+  if (a >= ldexp(1.0, -6)) {
+    (void)frexp(a, &e); /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;             /* a in [2^e, 2^(e+1)) */
+  }
+  double step = ldexp(1.0, e - 3);
+  double v = round_half_even(a / step) * step; /* a / step is exact: step is a power of 2 */
+  int efield = 0, mant = 0;
+  if (v >= ldexp(1.0, -6)) {
+    int ev;
+    double f = frexp(v, &ev); /* v = f * 2^ev = (2f) * 2^(ev-1) */
+    efield = ev - 1 + 7;
+    mant = (int)((2.0 * f - 1.0) * 8.0);
+  } else {
+    mant = (int)(v / ldexp(1.0, -9));
+  }
+  return (uint8_t)((sign << 7) | (efield << 3) | mant);
+}
+
+/* Append every sequence's q_lens[b] new rows of k_new / v_new ([B, max_q_len, Hkv, D] in
+ * q_dtype) into k_cache / v_cache ([num_blocks, block_size, Hkv, D] in kv_dtype), and for
+ * per-token fp8 their scales into k_scale / v_scale ([num_blocks, block_size, Hkv]).  For
+ * per-tensor fp8, k_scale[0] / v_scale[0] are read.  Nothing is written when a length or a
+ * block id in use is invalid: returns -3 (lengths) or -1 (block id), 0 otherwise. */
+int oracle_append_kv(const oracle_cfg *c, const void *k_new, const void *v_new,
+                     const int32_t *block_tables, const int32_t *context_lens,
+                     const int32_t *q_lens, void *k_cache, void *v_cache, float *k_scale,
+                     float *v_scale) {
+  int rc = check_lengths(c, context_lens, q_lens);
+  if (rc) return rc;
+  int bs = c->block_size, D = c->head_dim, H = c->num_kv_heads;
+  for (int b = 0; b < c->batch; ++b) {
+    int n = context_lens[b], ql = q_lens[b];
+    for (int i = 0; i < ql; ++i) {
+      int pos = n - ql + i;
+      int page = block_tables[(size_t)b * c->max_blocks_per_seq + pos / bs];
+      if (page < 0 || page >= c->num_blocks) return -1;
+    }
+  }
+  float *x = (float *)malloc(sizeof(float) * (size_t)D);
+  if (!x) return -2;
+  for (int b = 0; b < c->batch; ++b) {
+    int n = context_lens[b], ql = q_lens[b];
+    for (int i = 0; i < ql; ++i) {
+      int pos = n - ql + i;
+      int page = block_tables[(size_t)b * c->max_blocks_per_seq + pos / bs];
+      int slot = pos % bs;
+      for (int g = 0; g < H; ++g) {
+        size_t src = (((size_t)b * c->max_q_len + i) * H + g) * (size_t)D;
+        size_t row = ((size_t)page * bs + slot) * H + g;
+        for (int t = 0; t < 2; ++t) { /* K, then V */
+          const void *nw = t ? v_new : k_new;
+          void *cache = t ? v_cache : k_cache;
+          float *scales = t ? v_scale : k_scale;
+          if (c->kv_dtype != OR_E4M3) {
+            memcpy((uint16_t *)cache + row * D, (const uint16_t *)nw + src, sizeof(uint16_t) * D);
+            continue;
+          }
+          for (int d = 0; d < D; ++d) x[d] = (float)element(c->q_dtype, nw, src + d);
+          float s = 1.0f;
+          if (c->scale_mode == OR_SCALE_TOKEN) {
+            float amax = 0.0f;
+            for (int d = 0; d < D; ++d)
+              if (fabsf(x[d]) > amax) amax = fabsf(x[d]);
+            s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[row] = s;
+          } else if (c->scale_mode == OR_SCALE_TENSOR) {
+            s = scales[0];
+          }
+          uint8_t *codes = (uint8_t *)cache + row * D;
+          for (int d = 0; d < D; ++d) codes[d] = oracle_e4m3_encode(x[d] / s);
+        }
+      }
+    }
+  }
+  free(x);
+  return 0;
+}

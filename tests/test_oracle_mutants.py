@@ -7,6 +7,7 @@ import os
 import pytest
 
 import oracle
+import test_append_oracle as apins
 import test_oracle as pins
 from oracle.build import SRC, build
 
@@ -37,6 +38,21 @@ MUTANTS = {
         "return (real)s[((size_t)page * c->block_size + slot) * c->num_kv_heads];"),
     "v_scaled_by_k_scale": ("real vs = row_scale(p, 1, page, slot, g);",
                             "real vs = row_scale(p, 0, page, slot, g);"),
+    # quantise-on-write append
+    "append_wrong_slot": ("      int slot = pos % bs;\n", "      int slot = (pos + 1) % bs;\n"),
+    "append_position_ignores_q_len": (
+        "int pos = n - ql + i;\n      int page = block_tables[(size_t)b * c->max_blocks_per_seq + pos / bs];\n      int slot",
+        "int pos = n - 1 - i;\n      int page = block_tables[(size_t)b * c->max_blocks_per_seq + pos / bs];\n      int slot"),
+    "append_scale_divisor": ("s = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                             "s = amax > 0.0f ? amax / 447.0f : 1.0f;"),
+    "append_zero_row_scale": ("s = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                              "s = amax > 0.0f ? amax / 448.0f : 0.0f;"),
+    "append_v_uses_k_scale": ("float *scales = t ? v_scale : k_scale;",
+                              "float *scales = t ? k_scale : k_scale;"),
+    "append_tensor_scale_ignored": ("s = scales[0];", "s = 1.0f;"),
+    "encode_ties_away_from_zero": ("(fr == 0.5 && fmod(fl, 2.0) == 1.0)", "(fr == 0.5)"),
+    "encode_no_clamp": ("if (a > 448.0) a = 448.0;", ""),
+    "encode_subnormal_step": ("  int e = -6;\n", "  int e = -7;\n"),
 }
 
 
@@ -53,6 +69,14 @@ def _pins():
         out.append((f"brute{ci}",
                     lambda ci=ci: pins.test_oracle_matches_contiguous_brute_force(ci, "f64")))
     out.append(("split3", lambda: pins.test_split_invariance(3, "f64")))
+    for i in range(5):
+        out.append((f"append_golden{i}", lambda i=i: apins.test_golden_append_cases(i, "f64")))
+    out.append(("append_encode_grid",
+                apins.test_e4m3_encode_matches_torch_on_grid_midpoints_and_neighbours))
+    for mode in ("token", "tensor", "none"):
+        out.append((f"append_fp8_{mode}",
+                    lambda mode=mode: apins.test_fp8_append_codes_and_scales(mode, "bf16")))
+    out.append(("append_16bit", lambda: apins.test_16bit_append_places_rows_bitwise("bf16", "bf16")))
     out.append(("zero_scale", lambda: pins.test_zero_scale_gives_mean_over_visible_keys("f64")))
     return out
 
