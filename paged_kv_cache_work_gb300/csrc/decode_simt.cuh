@@ -481,12 +481,9 @@ cudaError_t launch_simt_instance(const KernelParams& prm, const CUtensorMap& kma
                                  const CUtensorMap& vmap, int grid, cudaStream_t s) {
   using T = SimtTraits<D, MP, KVK, TOKS>;
   auto kern = decode_simt_kernel<D, MP, KVK, QK, TOKS>;
-  static bool attr_set = false;  // benign race: every caller sets the same value
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};  // devices whose limit is raised
+  const cudaError_t e = set_smem_attr_once(attr_done, reinterpret_cast<const void*>(kern), T::SMEM);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(T::NTHREADS);

@@ -1,36 +1,39 @@
 // Fifth-generation tensor-core decode (tcgen05, accumulators in tensor memory) for large
 // query tiles: 33 to 128 query rows per kv head, 16-bit caches of head dim 128 or 256 and
-// fp8 caches of head dim 128 with per-tensor or no scales.
+// fp8 caches of head dim 128 with per-tensor, per-token or no scales.
 //
 // A step is a tile of 64 tokens.  The CTA is split into roles that talk only through
 // mbarriers, so copies, MMAs and the softmax of different steps overlap:
-//   warp 0      streams the items' K and V tiles through two TMA rings (TcProducer) of
-//               96 KB each: a K slot is released by the S that read it and a V slot by its
-//               PV, and K is copied one step ahead of V;
+//   warp 0      streams the items' K and V tiles through two TMA rings (TcProducer), K one
+//               step ahead of V, and, for per-token fp8 scales, each step's 64 K and 64 V
+//               scales into a small shared-memory ring of their own;
 //   warp 1      one thread issues, per step g, S = Q K^T (M = 128, N = 64, K = head dim)
 //               into tensor-memory buffer g % NSP, and then O += P V for step g - LAG
-//               (M = 128, N = head dim, K = 64, V read as an MN-major operand), so the
-//               in-order tensor pipe holds the next logits ahead of any PV that waits for
-//               the softmax;
-//   warps 2-5   one query row per thread: load the row's logits with tcgen05.ld, online
-//               softmax in registers (a row never leaves its thread), write the row of P as
-//               16-bit pairs over the first half of the same logits buffer; at the end of an
-//               item load O from tensor memory and write the output or the split partial
+//               (M = 128, N = head dim, K = 64, V read as an MN-major operand);
+//   warps 2-5   the softmax: tensor-memory lane L is owned by one thread, which loads its
+//               logits with tcgen05.ld, runs the online softmax in registers and writes its
+//               row of P as 16-bit pairs over the first half of the same logits buffer; at
+//               the end of an item it loads O and writes the output or the split partial
 //               (merge protocol of decode_common.cuh);
-//   warps 6-9   (fp8 caches) widen each step's e4m3 K rows to f16 in one of three
-//               shared-memory buffers, released by the step's S, and its V rows in one of
-//               four, released by its PV (one warp per SM sub-partition: with fewer, the
-//               conversion rate, not the copy, bounds the kernel).
-// Buffer g % NSP holds S(g) and then P(g) until the PV of step g has read it, so the MMA
-// thread waits for that PV before it writes S(g + NSP) there: NSP = 4 at head dim 128 and
-// 2 at head dim 256, as many as tensor memory holds next to O and the query rows (Q, as
-// 16-bit pairs: lane = row).  Shared memory carries only K and V (and, for fp8, their f16
-// widening).
+//   warps 6-9   (fp8 caches) widen each step's e4m3 K and V rows to f16 operands in shared
+//               memory (one warp per SM sub-partition).
 //
-// A tcgen05.mma of K = 16 occupies the tensor pipe about equally long at every N up to
-// 256, so these N = 64 logits use a quarter of its peak: at head dim 256 (16 S MMAs and 4
-// PV MMAs per 64 KB of cache) the pipe keeps up with HBM, at head dim 128 it is close to
-// being the limit.
+// Issue cost.  The tensor pipe takes about 48 SM clocks for an N = 64 logits MMA and 64 for
+// an N = 128 one when they are issued back to back, but each tcgen05.commit costs it about
+// 90 clocks more, and a wait for an MMA's completion right after issuing it drains the pipe
+// (measured on GB300 with standalone issue probes).  So every buffer is indexed by the step
+// modulo NSP, the number of S/P buffers, wherever shared memory allows: the commit that
+// tells the softmax its logits are ready also frees the step's K slot (or widened K
+// buffer), and the commit that ends a PV also frees its V slot: two commits per step.  And
+// the PV of step g trails its S by LAG = NSP - 2 steps where NSP >= 4, so the S that reuses
+// a buffer waits for a PV issued a step earlier, with MMAs still queued behind it.
+//
+// Query tiles of 64 rows (head dim 128) run as two token streams: rows 64-127 of the MMA
+// repeat rows 0-63 (the query rows are loaded twice), the thread of lane r < 64 takes the
+// first 32 tokens of every step and the thread of lane r + 64 the last 32, each with its own
+// running max and sum (the other half of its row of P is zero), so the softmax runs on all
+// four SM sub-partitions with half the exponentials per thread.  At the end of an item the
+// two streams of a row are merged with the log-sum-exp rule through shared memory.
 #pragma once
 
 #include "decode_common.cuh"
@@ -42,7 +45,7 @@ struct TcTraits {
   static constexpr int D = D_;    // 128 or 256
   static constexpr int MP = MP_;  // query rows of a unit; the MMA always has M = 128
   static constexpr int KVK = KVK_;
-  static constexpr bool TOKS = TOKS_;
+  static constexpr bool TOKS = TOKS_;  // per-token fp8 scales
   static constexpr bool FP8 = KVK == KV_FP8;
   static constexpr int BPE = FP8 ? 1 : 2;
   static constexpr int W_PROD = 0, W_MMA = 1, W_SOFT = 2, W_CONV = 6;
@@ -51,50 +54,64 @@ struct TcTraits {
   static constexpr int NTHREADS = NW * 32;
   static constexpr int TT = kTcStepTokens;  // tokens per tile and per MMA step: 64
   static constexpr int SUB = TT;
+  // two token streams per query row (64-row tiles of head dim 128)
+  static constexpr bool DUAL = MP == 64 && D == 128;
+  static constexpr int NL = DUAL ? SUB / 2 : SUB;  // logits of a step per softmax thread
+  // S/P buffers in tensor memory and how many steps a PV trails its S
+  static constexpr int NSP = D == 256 ? 2 : (FP8 ? 4 : 5);
+  static constexpr int LAG = NSP >= 4 ? NSP - 2 : NSP - 1;
   static constexpr int KTILE = TT * D * BPE;  // 16 KB, 32 KB at head dim 256, 8 KB for fp8
-  static constexpr int SLOT = KTILE;  // a ring slot
-  static constexpr int NSTAGE = FP8 ? 5 : 98304 / KTILE;  // slots of each ring: 6, 3 or 5
+  static constexpr int SLOT = KTILE;          // a ring slot
+  // Slots of each TMA ring.  16-bit caches of head dim 128: NSP, so that slot g % NSP is
+  // released by the commit of the S (K) or the PV (V) of step g that the softmax and the MMA
+  // thread wait for anyway.  Head dim 256: three slots (two S/P buffers fit in tensor
+  // memory, two slots would leave too little in flight), released by commits of their own.
+  // fp8: three slots of codes, released by the widening warps.
+  static constexpr int NRING = FP8 ? 3 : (D == 256 ? 3 : NSP);
+  static constexpr bool RING_BY_MMA = !FP8 && NRING == NSP;
   static constexpr int ROWB = 128;             // swizzled slabs of 128 bytes per row
   static constexpr int NSLAB = D * BPE / 128;  // slabs of a cache tile row
-  // S/P buffers in tensor memory: four at head dim 128 (S(g) waits only for the PV of
-  // step g - 4), two at 256
-  static constexpr int NSP = D == 128 ? 4 : 2;
-  static constexpr int OFF_K = 0;                      // K ring: NSTAGE slots
-  static constexpr int OFF_V = OFF_K + NSTAGE * SLOT;  // V ring: NSTAGE slots
-  // fp8: the widened (f16) K rows of NCK steps and V rows of NCV steps, each a
-  // 128-byte-swizzled operand of two 64-dim slabs (a K buffer is released by its S, a V
-  // buffer by its PV)
-  static constexpr int NCK = FP8 ? 3 : 0;
-  static constexpr int NCV = FP8 ? 4 : 0;
+  static constexpr int OFF_K = 0;                      // K ring
+  static constexpr int OFF_V = OFF_K + NRING * SLOT;   // V ring
+  // fp8: the widened (f16) K and V rows of NSP steps each, 128-byte-swizzled operands of two
+  // 64-dim slabs; the K buffer of step g is released by its S, the V buffer by its PV
+  static constexpr int NCB = FP8 ? NSP : 0;
   static constexpr int CV_SLAB = SUB * 128;
   static constexpr int CV_BUF = 2 * CV_SLAB;
-  static constexpr int OFF_CV = OFF_V + NSTAGE * SLOT;  // K buffers, then V buffers
+  static constexpr int OFF_CV = OFF_V + NRING * SLOT;  // K buffers, then V buffers
   static constexpr int SCRATCH = OFF_CV;  // bytes free for the merges at the end (the rings)
-  static constexpr int LAG = NSP - 1;  // steps a PV trails its S
   static constexpr int KSLAB = FP8 ? CV_SLAB : TT * 128;  // slab stride of the MMA operands
-  static constexpr int OFF_ML = OFF_CV + (NCK + NCV) * CV_BUF;
-  static constexpr int ML_BYTES = round_up(2 * MP * 4, 128);
+  // two-stream merge: the second stream's O rows (fp32, 16-byte chunks swizzled by row)
+  static constexpr int OFF_MRG = OFF_CV + 2 * NCB * CV_BUF;
+  static constexpr int MRG_BYTES = DUAL ? 64 * D * 4 : 0;
+  // per-token scales: NSC slots of 64 K then 64 V fp32 scales
+  static constexpr int NSC = TOKS ? 8 : 0;
+  static constexpr int SC_SLOT = 2 * TT * 4;
+  static constexpr int OFF_SC = OFF_MRG + MRG_BYTES;
+  static constexpr int OFF_ML = OFF_SC + NSC * SC_SLOT;
+  static constexpr int ML_BYTES = round_up(2 * MP * 4 + (DUAL ? 2 * 64 * 4 : 0), 128);
   static constexpr int OFF_BAR = round_up(OFF_ML + ML_BYTES, 64);
-  // full_k, empty_k, full_v, empty_v (NSTAGE each), s_full, p_full, pv_done (NSP each),
-  // o_free, q_full, mma_end, full and free of the K buffers and of the V buffers
-  static constexpr int NBAR = 4 * NSTAGE + 3 * NSP + 3 + 2 * (NCK + NCV);
+  // full_k, empty_k, full_v, empty_v (NRING each), s_full, p_full, pv_done (NSP each),
+  // o_free, q_full, mma_end, ck_full and cv_full (NCB each), sc_full and sc_free (NSC each)
+  static constexpr int NBAR = 4 * NRING + 3 * NSP + 3 + 2 * NCB + 2 * NSC;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 16 + 1024;
   static constexpr int CTAS_PER_SM = 1;
   // Tensor memory (lane = query row, 32-bit columns): NSP S/P buffers of SUB fp32 columns
   // (P, SUB / 2 columns of 16-bit pairs, overwrites the first half of its own S), O (D fp32
-  // columns) and Q (D / 2 columns of 16-bit pairs).  Head dim 128: S/P [0, 256), O
-  // [256, 384), Q [384, 448).  Head dim 256: S/P [0, 128), Q [128, 256), O [256, 512).
+  // columns) and Q (D / 2 columns of 16-bit pairs).  Head dim 128: S/P [0, 64 NSP), O
+  // [64 NSP, 64 NSP + 128), Q after O.  Head dim 256: S/P [0, 128), Q [128, 256),
+  // O [256, 512).
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = D == 256 ? 256 : NSP * SUB;
   static constexpr uint32_t COL_Q = D == 256 ? NSP * SUB : COL_O + D;
   static_assert(NSP * SUB + D + D / 2 <= (int)TMEM_COLS, "tensor memory");
-  static_assert(!TOKS, "per-token scales stay on the mma.sync kernel");
+  static_assert(!TOKS || FP8, "per-token scales belong to fp8 caches");
   static_assert(!FP8 || D == 128, "fp8 caches at head dim 128");
-  static_assert(!FP8 || (SUB * 8) % (32 * NCW) == 0, "widening: whole passes");
-  // the V rows of step g wait for the PV of step g - NCV, issued after the S of step
-  // g - NCV + LAG, which waits for the K rows of that step: the widening, K(g) then V(g),
+  static_assert(!FP8 || (SUB * 8) % (32 * (NCW > 0 ? NCW : 1)) == 0, "widening: whole passes");
+  // the V rows of step g wait for the PV of step g - NSP, issued after the S of step
+  // g - NSP + LAG, which waits for the K rows of that step: the widening, K(g) then V(g),
   // must not need K rows past g
-  static_assert(LAG < NSP && (!FP8 || LAG <= NCV), "no cycle between the roles");
+  static_assert(LAG >= 1 && LAG < NSP, "no cycle between the roles");
   static_assert(MP == 64 || MP == 128, "row tile");
   static_assert(D == 128 || D == 256, "head dim");
   static_assert(SUB == 64, "step");
@@ -261,98 +278,144 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 #pragma unroll
   for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
 }
-
 // The TMA side of the tcgen05 kernel, run by warp 0 (all lanes, same state).  Tile n of the
-// CTA's work list goes to slot n % NSTAGE of the K ring and of the V ring; lane
+// CTA's work list goes to slot n % NRING of the K ring and of the V ring; lane
 // page * NSLAB + slab copies one 128-byte column slab of one page of the tile.  The order of
-// the copies is K(0), K(1), V(0), K(2), V(1), ...: a copy waits until the tile NSTAGE
+// the copies is K(0), K(1), V(0), K(2), V(1), ...: a copy waits until the tile NRING
 // earlier has been read from its slot (by its S for K and its PV for V, or, for fp8, by the
-// widening warps).
+// widening warps).  Per-token scales of tile n go to slot n % NSC of the scale ring, which
+// the softmax releases.
+//
+// The warp issues a tile's copies every few hundred clocks, so nothing on its path may wait
+// on memory: the parameters it uses live in registers, and each lane's block id is looked
+// up two tiles before its copy is issued (and not at all while the tile stays on the page of
+// the previous one).
 template <class T>
 struct TcProducer {
   struct Box {
-    int blk, row, g;
+    int blk, row, g, tok0, t1;
     bool ok;
     uint32_t nvalid;
   };
-  const KernelParams* p;
+  // a tile whose block id (this lane's page) is being fetched
+  struct Ahead {
+    int b, g, tok0, t1, blk;
+    bool want, valid;
+  };
   const CUtensorMap* kmap;
   const CUtensorMap* vmap;
   char* smem;
-  uint64_t *full_k, *empty_k, *full_v, *empty_v;
+  uint64_t *full_k, *rel_k, *full_v, *rel_v, *sc_full, *sc_free;
   volatile int* abort_flag;
-  int lane, it, it_end, k, ntiles, t0, t1, b, g, box_rows, nbox, blk_next;
-  uint32_t box_bytes, nk, nv;
-  bool have, next_ready;
+  int32_t* flags;
+  const int32_t* bt;
+  const int4* items;
+  const float* kscale;
+  const float* vscale;
+  int maxb, bs, bs_shift, nblocks, Hkv, RB;
+  int lane, box_rows, nbox;
+  uint32_t box_bytes, nk, nv, nsc;
+  bool scale_bulk;  // a tile's scales are two contiguous 256-byte runs (one kv head, big pages)
+  // walk over the work list (the tile after the two being fetched)
+  int it, it_end, k, ntiles, t0, t1, b, g;
+  bool have;
   int4 item_next;
-
-  __device__ __forceinline__ int block_of(int bb, int tt0, int tt1, int kk) const {
-    const int tokb = tt0 + kk * T::TT + (lane / T::NSLAB) * box_rows;
-    return (lane < nbox * T::NSLAB && tokb < tt1)
-               ? __ldg(p->bt + (size_t)bb * p->maxb + (tokb >> p->bs_shift))
-               : -1;
-  }
+  int last_b, last_page, last_blk;  // this lane's previous lookup
+  Ahead q0, q1;
 
   __device__ __forceinline__ void init(const KernelParams* prm, const CUtensorMap* km,
                                        const CUtensorMap* vm, char* sm, uint64_t* fk,
-                                       uint64_t* ek, uint64_t* fv, uint64_t* ev,
-                                       volatile int* ab, int ln, int ib, int ie) {
-    p = prm; kmap = km; vmap = vm; smem = sm; full_k = fk; empty_k = ek; full_v = fv;
-    empty_v = ev; abort_flag = ab; lane = ln; it = ib - 1; it_end = ie; k = 0; ntiles = 0;
-    box_rows = min(p->bs, T::TT);
+                                       uint64_t* rk, uint64_t* fv, uint64_t* rv, uint64_t* scf,
+                                       uint64_t* scr, volatile int* ab, int ln, int ib, int ie) {
+    kmap = km; vmap = vm; smem = sm; full_k = fk; rel_k = rk; full_v = fv; rel_v = rv;
+    sc_full = scf; sc_free = scr; abort_flag = ab; lane = ln;
+    flags = prm->flags; bt = prm->bt; items = prm->items; kscale = prm->k_scale;
+    vscale = prm->v_scale; maxb = prm->maxb; bs = prm->bs; bs_shift = prm->bs_shift;
+    nblocks = prm->nblocks; Hkv = prm->Hkv; RB = prm->RB;
+    box_rows = min(bs, T::TT);
     nbox = T::TT / box_rows;
     box_bytes = (uint32_t)box_rows * T::ROWB;
-    nk = nv = 0;
-    have = next_ready = false;
-    blk_next = -1;
-    item_next = ib < ie ? p->items[ib] : make_int4(0, 0, 0, -1);
+    scale_bulk = T::TOKS && Hkv == 1 && box_rows == T::TT &&
+                 ((reinterpret_cast<uintptr_t>(kscale) | reinterpret_cast<uintptr_t>(vscale)) & 15) == 0;
+    nk = nv = nsc = 0;
+    it = ib - 1;
+    it_end = ie;
+    have = false;
+    item_next = ib < ie ? items[ib] : make_int4(0, 0, 0, -1);
+    last_b = -1;
+    last_page = -1;
+    last_blk = -1;
+    fetch(q0);
+    fetch(q1);
   }
 
-  // This lane's box of the next tile of the list; false when the list is exhausted.  The
-  // block id of the tile after it is loaded here too, to land during the waits.
-  __device__ __forceinline__ bool next_tile(Box& bx) {
+  // The next tile of the work list into a, with this lane's block id lookup started.
+  __device__ __forceinline__ void fetch(Ahead& a) {
     while (!have) {
-      if (++it >= it_end) return false;
+      if (++it >= it_end) {
+        a.valid = false;
+        return;
+      }
       const int4 item = item_next;
-      if (it + 1 < it_end) item_next = p->items[it + 1];
+      if (it + 1 < it_end) item_next = items[it + 1];
       t0 = item.y;
       t1 = item.z;
       if (t1 <= t0) continue;
-      b = item.x / (p->Hkv * p->RB);
-      g = (item.x / p->RB) % p->Hkv;
+      b = item.x / (Hkv * RB);
+      g = (item.x / RB) % Hkv;
       k = 0;
       ntiles = ceil_div(t1 - t0, T::TT);
-      if (!next_ready) blk_next = block_of(b, t0, t1, 0);
-      next_ready = false;
       have = true;
     }
-    const int tokb = t0 + k * T::TT + (lane / T::NSLAB) * box_rows;
-    const bool want = lane < nbox * T::NSLAB && tokb < t1;
-    bx.blk = blk_next;
-    bx.ok = want && blk_next >= 0 && blk_next < p->nblocks;
-    if (want && !bx.ok) atomicOr(p->flags, PA_FLAG_BAD_BLOCK_ID);
-    bx.nvalid = __popc(__ballot_sync(kFull, bx.ok));
-    bx.row = tokb & (p->bs - 1);
-    bx.g = g;
-    if (k + 1 < ntiles) {
-      blk_next = block_of(b, t0, t1, k + 1);
-    } else if (it + 1 < it_end && item_next.z > item_next.y) {
-      blk_next = block_of(item_next.x / (p->Hkv * p->RB), item_next.y, item_next.z, 0);
-      next_ready = true;
-    }
+    a.valid = true;
+    a.b = b;
+    a.g = g;
+    a.tok0 = t0 + k * T::TT;
+    a.t1 = t1;
     if (++k >= ntiles) have = false;
+    const int tokb = a.tok0 + (lane / T::NSLAB) * box_rows;
+    a.want = lane < nbox * T::NSLAB && tokb < a.t1;
+    a.blk = -1;
+    if (a.want) {
+      const int page = tokb >> bs_shift;
+      if (a.b != last_b || page != last_page) {
+        last_blk = __ldg(bt + (size_t)a.b * maxb + page);
+        last_b = a.b;
+        last_page = page;
+      }
+      a.blk = last_blk;
+    }
+  }
+
+  // This lane's box of the next tile of the list; false when the list is exhausted.
+  __device__ __forceinline__ bool next_tile(Box& bx) {
+    if (!q0.valid) return false;
+    bx.tok0 = q0.tok0;
+    bx.t1 = q0.t1;
+    bx.g = q0.g;
+    bx.blk = q0.blk;
+    bx.ok = q0.want && q0.blk >= 0 && q0.blk < nblocks;
+    if (q0.want && !bx.ok) atomicOr(flags, PA_FLAG_BAD_BLOCK_ID);
+    bx.nvalid = __popc(__ballot_sync(kFull, bx.ok));
+    bx.row = (q0.tok0 + (lane / T::NSLAB) * box_rows) & (bs - 1);
+    q0 = q1;
+    fetch(q1);
     return true;
   }
 
-  // Copy a tile's boxes into slot n % NSTAGE of one ring once the slot is released.
+  __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity) {
+    if (mbar_wait(bar, parity, abort_flag)) return true;
+    atomicOr(flags, PA_FLAG_WAIT_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+  }
+
+  // Copy a tile's boxes into slot n % NRING of one ring once the slot is released (the
+  // release barrier completes once per use of the slot, in tile order).
   __device__ __forceinline__ bool issue(const Box& bx, uint32_t n, uint64_t* full,
-                                        uint64_t* empty, const CUtensorMap* map, int ring) {
-    const int s = (int)(n % T::NSTAGE);
-    if (!mbar_wait(&empty[s], ((n / T::NSTAGE) & 1) ^ 1, abort_flag)) {
-      atomicOr(p->flags, PA_FLAG_WAIT_TIMEOUT);
-      *abort_flag = 1;
-      return false;
-    }
+                                        uint64_t* rel, const CUtensorMap* map, int ring) {
+    const int s = (int)(n % T::NRING);
+    if (!wait_or_abort(&rel[s], ((n / T::NRING) & 1) ^ 1)) return false;
     if (lane == 0) mbar_arrive_expect_tx(&full[s], bx.nvalid * box_bytes);
     __syncwarp();
     char* slot = smem + ring + s * T::SLOT;
@@ -365,18 +428,65 @@ struct TcProducer {
     return true;
   }
 
+  // The K and V scales of tile n's tokens into scale slot n % NSC, completing on sc_full
+  // (32 arrivals: one per lane).  One kv head and pages of at least a tile: the tile's scales
+  // are two contiguous 256-byte runs, copied by two bulk copies; otherwise 4-byte cp.async,
+  // two tokens a lane.  Tokens past the item or on a bad page keep a stale value: the softmax
+  // masks them.
+  __device__ __forceinline__ bool issue_scales(const Box& bx, uint32_t n) {
+    if constexpr (T::TOKS) {
+      const int s = (int)(n % T::NSC);
+      if (!wait_or_abort(&sc_free[s], ((n / T::NSC) & 1) ^ 1)) return false;
+      float* ks = reinterpret_cast<float*>(smem + T::OFF_SC + s * T::SC_SLOT);
+      float* vs = ks + T::TT;
+      if (scale_bulk) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&sc_full[s], bx.ok ? 2u * T::TT * 4 : 0u);
+          if (bx.ok) {  // lane 0's box is the tile's one page
+            const size_t idx = (size_t)bx.blk * bs + bx.row;
+            bulk_load_1d(ks, kscale + idx, T::TT * 4, &sc_full[s]);
+            bulk_load_1d(vs, vscale + idx, T::TT * 4, &sc_full[s]);
+          }
+        } else {
+          mbar_arrive(&sc_full[s]);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = lane + 32 * h;
+          const int src = (t / box_rows) * T::NSLAB;  // the lane holding the page's block id
+          const int blk = __shfl_sync(kFull, bx.blk, src);
+          const bool ok = __shfl_sync(kFull, bx.ok ? 1 : 0, src) != 0;
+          const int tok = bx.tok0 + t;
+          if (ok && tok < bx.t1) {
+            const size_t idx = ((size_t)blk * bs + (tok & (bs - 1))) * Hkv + bx.g;
+            cp_async_4(ks + t, kscale + idx);
+            cp_async_4(vs + t, vscale + idx);
+          }
+        }
+        cp_async_arrive_noinc(&sc_full[s]);
+      }
+    }
+    return true;
+  }
+
+  // K (and the scales) of a tile, counted as soon as each copy is in flight
+  __device__ __forceinline__ bool issue_k(const Box& bx) {
+    if (!issue(bx, nk, full_k, rel_k, kmap, T::OFF_K)) return false;
+    ++nk;
+    if (!issue_scales(bx, nsc)) return false;
+    ++nsc;
+    return true;
+  }
+
   __device__ __forceinline__ void run() {
     Box cur, nxt;
     if (!next_tile(cur)) return;
-    if (!issue(cur, nk, full_k, empty_k, kmap, T::OFF_K)) return;
-    ++nk;
+    if (!issue_k(cur)) return;
     while (true) {
       const bool more = next_tile(nxt);
-      if (more) {
-        if (!issue(nxt, nk, full_k, empty_k, kmap, T::OFF_K)) return;
-        ++nk;
-      }
-      if (!issue(cur, nv, full_v, empty_v, vmap, T::OFF_V)) return;
+      if (more && !issue_k(nxt)) return;
+      if (!issue(cur, nv, full_v, rel_v, vmap, T::OFF_V)) return;
       ++nv;
       if (!more) return;
       cur = nxt;
@@ -385,10 +495,15 @@ struct TcProducer {
 
   // Let every copy this warp started land before the CTA may exit.
   __device__ __forceinline__ void drain() {
-    for (uint32_t j = nk > (uint32_t)T::NSTAGE ? nk - T::NSTAGE : 0; j < nk; ++j)
-      mbar_wait_drain(&full_k[j % T::NSTAGE], (j / T::NSTAGE) & 1);
-    for (uint32_t j = nv > (uint32_t)T::NSTAGE ? nv - T::NSTAGE : 0; j < nv; ++j)
-      mbar_wait_drain(&full_v[j % T::NSTAGE], (j / T::NSTAGE) & 1);
+    if constexpr (T::TOKS) {
+      cp_async_wait_all();
+      for (uint32_t j = nsc > (uint32_t)T::NSC ? nsc - T::NSC : 0; j < nsc; ++j)
+        mbar_wait_drain(&sc_full[j % T::NSC], (j / T::NSC) & 1);
+    }
+    for (uint32_t j = nk > (uint32_t)T::NRING ? nk - T::NRING : 0; j < nk; ++j)
+      mbar_wait_drain(&full_k[j % T::NRING], (j / T::NRING) & 1);
+    for (uint32_t j = nv > (uint32_t)T::NRING ? nv - T::NRING : 0; j < nv; ++j)
+      mbar_wait_drain(&full_v[j % T::NRING], (j / T::NRING) & 1);
   }
 };
 
@@ -399,6 +514,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   using T = TcTraits<D_, MP, KVK, TOKS>;
   constexpr int SUB = T::SUB;
   constexpr int D = T::D;
+  constexpr int NSP = T::NSP;
   constexpr bool BF = KVK == KV_BF16;  // MMA operands bf16 (else f16: f16 and fp8 caches)
   constexpr uint32_t ID_S = umma_idesc(128, SUB, BF, false);
   constexpr uint32_t ID_PV = umma_idesc(128, D, BF, true);
@@ -406,20 +522,20 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   extern __shared__ char smem_raw[];
   char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint64_t* full_k = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
-  uint64_t* empty_k = full_k + T::NSTAGE;
-  uint64_t* full_v = empty_k + T::NSTAGE;
-  uint64_t* empty_v = full_v + T::NSTAGE;
-  uint64_t* s_full = empty_v + T::NSTAGE;  // [NSP]
-  uint64_t* p_full = s_full + T::NSP;      // [NSP]: P of the step in buffer b is written
-  uint64_t* pv_done = p_full + T::NSP;     // [NSP]: the PV that read buffer b has completed
-  uint64_t* o_free = pv_done + T::NSP;
+  uint64_t* empty_k = full_k + T::NRING;
+  uint64_t* full_v = empty_k + T::NRING;
+  uint64_t* empty_v = full_v + T::NRING;
+  uint64_t* s_full = empty_v + T::NRING;  // [NSP]: S of the step in buffer b is complete
+  uint64_t* p_full = s_full + NSP;        // [NSP]: P of the step in buffer b is written
+  uint64_t* pv_done = p_full + NSP;       // [NSP]: the PV that read buffer b has completed
+  uint64_t* o_free = pv_done + NSP;
   uint64_t* q_full = o_free + 1;
   uint64_t* mma_end = q_full + 1;
-  uint64_t* ck_full = mma_end + 1;       // [NCK]: widened K rows of the step in buffer b
-  uint64_t* ck_free = ck_full + T::NCK;  // [NCK]: the S that read buffer b has completed
-  uint64_t* cv_full = ck_free + T::NCK;  // [NCV]: widened V rows of the step in buffer b
-  uint64_t* cv_free = cv_full + T::NCV;  // [NCV]: the PV that read buffer b has completed
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(cv_free + T::NCV);
+  uint64_t* ck_full = mma_end + 1;       // [NCB]: widened K rows of the step in buffer b
+  uint64_t* cv_full = ck_full + T::NCB;  // [NCB]: widened V rows of the step in buffer b
+  uint64_t* sc_full = cv_full + T::NCB;  // [NSC]: per-token scales of the step in slot b
+  uint64_t* sc_free = sc_full + T::NSC;  // [NSC]: the softmax is done with slot b
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sc_free + T::NSC);
   volatile int* pend = abort_flag + 2;        // [4]: split pieces published, see finish_pending
   volatile int* cnt_seen_s = abort_flag + 6;  // published pieces of the item's unit, seen late
   uint32_t* tslot = reinterpret_cast<uint32_t*>(const_cast<int*>(abort_flag + 7));
@@ -427,25 +543,26 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < T::NSTAGE; ++s) {
+    for (int s = 0; s < T::NRING; ++s) {
       mbar_init(&full_k[s], 1);  // the expect_tx arrival of the copy
       mbar_init(&full_v[s], 1);
-      // readers: the commit of the S (K) or PV (V) that read the slot, or the fp8 widening
+      // readers of a ring slot: the widening warps (fp8), or the commit of the S (K) or PV
+      // (V) that read it when the ring is not released through s_full / pv_done
       mbar_init(&empty_k[s], T::FP8 ? T::NCW : 1);
       mbar_init(&empty_v[s], T::FP8 ? T::NCW : 1);
     }
-    for (int b = 0; b < T::NCK; ++b) {
+    for (int b = 0; b < T::NCB; ++b) {
       mbar_init(&ck_full[b], T::NCW);
-      mbar_init(&ck_free[b], 1);
-    }
-    for (int b = 0; b < T::NCV; ++b) {
       mbar_init(&cv_full[b], T::NCW);
-      mbar_init(&cv_free[b], 1);
     }
-    for (int b = 0; b < T::NSP; ++b) {
+    for (int b = 0; b < NSP; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 4);
       mbar_init(&pv_done[b], 1);
+    }
+    for (int b = 0; b < T::NSC; ++b) {
+      mbar_init(&sc_full[b], 32);  // one cp.async arrival per producer lane
+      mbar_init(&sc_free[b], 4);   // the four softmax warps
     }
     mbar_init(o_free, 4);
     mbar_init(q_full, 4);
@@ -486,8 +603,9 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   if (warp == T::W_PROD) {
     // ================================================================ TMA producer
     TcProducer<T> prod;
-    prod.init(&p, &kmap, &vmap, smem, full_k, empty_k, full_v, empty_v, abort_flag, lane,
-              it_begin, it_end);
+    prod.init(&p, &kmap, &vmap, smem, full_k, T::RING_BY_MMA ? s_full : empty_k, full_v,
+              T::RING_BY_MMA ? pv_done : empty_v, sc_full, sc_free, abort_flag, lane, it_begin,
+              it_end);
     prod.run();  // every tile of the work list, as slots come free
     prod.drain();
   } else if (warp == T::W_MMA) {
@@ -497,19 +615,19 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       uint32_t q_ph = 0, o_ph = 0;
       // step x uses buffer x % NSP; every barrier of a buffer completes once per use, in
       // step order, so the phase of step x is (x / NSP) & 1
-      // O += P V of step gp (its P, in buffer gp % NSP, must be written); the commit releases
-      // the V slot (fp8: the V buffer)
+      // O += P V of step gp (its P, in buffer gp % NSP, must be written); the commit to
+      // pv_done also releases the V slot (or the widened V buffer) of the step
       auto issue_pv = [&](uint32_t gp, bool first) {
-        const int slot = (int)(gp % T::NSTAGE);
         uint32_t vaddr;
         if constexpr (T::FP8) {
-          wait_bar(&cv_full[gp % T::NCV], (gp / T::NCV) & 1);
-          vaddr = smem_addr(smem + T::OFF_CV + (T::NCK + gp % T::NCV) * T::CV_BUF);
+          wait_bar(&cv_full[gp % NSP], (gp / NSP) & 1);
+          vaddr = smem_addr(smem + T::OFF_CV + (NSP + gp % NSP) * T::CV_BUF);
         } else {
+          const int slot = (int)(gp % T::NRING);
+          wait_bar(&full_v[slot], (gp / T::NRING) & 1);
           vaddr = smem_addr(smem + T::OFF_V + slot * T::SLOT);
-          wait_bar(&full_v[slot], (gp / T::NSTAGE) & 1);
         }
-        wait_bar(&p_full[gp % T::NSP], (gp / T::NSP) & 1);
+        wait_bar(&p_full[gp % NSP], (gp / NSP) & 1);
         if (first && items_done > 0) {  // the previous item's epilogue has read O
           wait_bar(o_free, o_ph);
           o_ph ^= 1u;
@@ -518,13 +636,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < SUB / 16; ++kk) {
           const uint64_t bd = umma_desc(vaddr + kk * 2048, T::KSLAB, 1024);
-          umma_f16_ta(t_o, t_s + (gp % T::NSP) * SUB + kk * 8, bd, ID_PV, !(first && kk == 0));
+          umma_f16_ta(t_o, t_s + (gp % NSP) * SUB + kk * 8, bd, ID_PV, !(first && kk == 0));
         }
-        umma_commit(&pv_done[gp % T::NSP]);
-        if constexpr (T::FP8)
-          umma_commit(&cv_free[gp % T::NCV]);
-        else
-          umma_commit(&empty_v[slot]);
+        umma_commit(&pv_done[gp % NSP]);
+        if constexpr (!T::FP8 && !T::RING_BY_MMA) umma_commit(&empty_v[gp % T::NRING]);
       };
       for (int it = it_begin; it < it_end; ++it) {
         const int4 item = p.items[it];
@@ -533,37 +648,35 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         const int nsub = ceil_div(t1 - t0, SUB);
         wait_bar(q_full, q_ph);  // the item's query rows are in tensor memory
         q_ph ^= 1u;
-        // the PVs trail the S MMAs by LAG steps, so the in-order tensor pipe always holds
-        // the logits of the next steps ahead of a PV that waits for the softmax (LAG < NSP:
-        // S(g) waits for the PV of step g - NSP, issued before it)
+        // the PVs trail the S MMAs by LAG steps, so the in-order tensor pipe holds the
+        // logits of the next steps ahead of a PV that waits for the softmax, and the S that
+        // reuses a buffer (after the PV of step g - NSP) finds MMAs still queued
         constexpr int LAG = T::LAG;
         const uint32_t g_item = g;  // the item's first step
         for (int j = 0; j < nsub; ++j, ++g) {
-          const int slot = (int)(g % T::NSTAGE);
           uint32_t kbase;
           if constexpr (T::FP8) {
-            wait_bar(&ck_full[g % T::NCK], (g / T::NCK) & 1);
-            kbase = smem_addr(smem + T::OFF_CV + (g % T::NCK) * T::CV_BUF);
+            wait_bar(&ck_full[g % NSP], (g / NSP) & 1);
+            kbase = smem_addr(smem + T::OFF_CV + (g % NSP) * T::CV_BUF);
           } else {
-            wait_bar(&full_k[slot], (g / T::NSTAGE) & 1);
+            const int slot = (int)(g % T::NRING);
+            wait_bar(&full_k[slot], (g / T::NRING) & 1);
             kbase = smem_addr(smem + T::OFF_K + slot * T::SLOT);
           }
-          if (g >= (uint32_t)T::NSP) {  // the buffer holds P(g - NSP) until its PV has read it
-            const uint32_t x = g - T::NSP;
-            wait_bar(&pv_done[x % T::NSP], (x / T::NSP) & 1);
+          if (g >= (uint32_t)NSP) {  // the buffer holds P(g - NSP) until its PV has read it
+            const uint32_t x = g - NSP;
+            wait_bar(&pv_done[x % NSP], (x / NSP) & 1);
           }
           tc_fence_after();
-          const uint32_t t_sg = t_s + (g % T::NSP) * SUB;
+          const uint32_t t_sg = t_s + (g % NSP) * SUB;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t bd = umma_desc(kbase + (kk >> 2) * T::KSLAB + (kk & 3) * 32, 16, 1024);
             umma_f16_ta(t_sg, t_q + kk * 8, bd, ID_S, kk > 0);
           }
-          umma_commit(&s_full[g % T::NSP]);
-          if constexpr (T::FP8)
-            umma_commit(&ck_free[g % T::NCK]);
-          else
-            umma_commit(&empty_k[slot]);
+          // the logits are ready; the K slot (or widened K buffer) of the step is free
+          umma_commit(&s_full[g % NSP]);
+          if constexpr (!T::FP8 && !T::RING_BY_MMA) umma_commit(&empty_k[g % T::NRING]);
           if (j >= LAG) issue_pv(g - LAG, j == LAG);
         }
         for (int j = nsub > LAG ? nsub - LAG : 0; j < nsub; ++j) issue_pv(g_item + j, j == 0);
@@ -574,20 +687,26 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     }
   } else if (warp < T::W_CONV) {
     // ================================================================ softmax and epilogue
-    const int stid = tid - T::W_SOFT * 32;            // 0 .. 127 over the four warps
-    const int r = 32 * (warp & 3) + lane;            // query row = this thread's TMEM lane
+    constexpr bool DUAL = T::DUAL;
+    constexpr int NL = T::NL;                       // logits of a step per thread
+    const int stid = tid - T::W_SOFT * 32;          // 0 .. 127 over the four warps
+    const int r = 32 * (warp & 3) + lane;           // this thread's tensor-memory lane
+    const int hs = DUAL ? (r >> 6) : 0;             // token stream: the step's tokens [NL hs, NL hs + NL)
+    const int qr = DUAL ? (r & 63) : r;             // query row of the unit's tile
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const bool tensor_scale = p.scale_mode == PA_SCALE_PER_TENSOR;
     const float kts = tensor_scale ? __ldg(p.k_scale) : 1.f;
     const float vts = tensor_scale ? __ldg(p.v_scale) : 1.f;
     const float qk_scale = p.qk_scale * kts;
+    float* mrg = reinterpret_cast<float*>(smem + T::OFF_MRG);  // [64][D], chunks swizzled
+    float* mrg_ml = mlbuf + 2 * MP;                             // [64][2]: m, l of stream 1
     uint32_t g = 0;
     uint32_t pv_next = 0;  // the first step whose PV completion is not consumed yet
     // wait until the PV of step x (which read buffer x % NSP) has completed; completions
     // are consumed in step order, and none is ever two ahead of its consumer on a buffer
     auto wait_pv_step = [&](uint32_t x) {
       for (; pv_next <= x; ++pv_next)
-        wait_bar(&pv_done[pv_next % T::NSP], (pv_next / T::NSP) & 1);
+        wait_bar(&pv_done[pv_next % NSP], (pv_next / NSP) & 1);
       tc_fence_after();
     };
     int2 pend_even = make_int2(-1, 0), pend_odd = make_int2(-1, 0);  // held by stid 0
@@ -603,13 +722,13 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       const bool in_dec = slot >= 0 && uinfo.y <= p.ns_dec;
       const int nsub = ceil_div(t1 - t0, SUB);
       int cnt_seen = -1;
-      const int rg = rb * MP + r;
-      const bool real = r < MP && rg < p.M;
+      const int rg = rb * MP + qr;
+      const bool real = qr < MP && rg < p.M;
       const int qi = real ? rg / p.G : 0, hq = g_kv * p.G + (real ? rg % p.G : 0);
       const int lim = (real && qi < ql) ? (p.causal ? n - ql + qi + 1 : n) : 0;
-      // a warp whose 32 rows hold no query (the upper half of a 64-row tile) skips the
-      // softmax; its rows of P and O are never read, and it keeps only the waits and
-      // arrivals that keep the barriers' phases in step
+      // a warp whose 32 rows hold no query (padding rows of a tile) skips the softmax; its
+      // rows of P and O are never read, and it keeps only the waits and arrivals that keep
+      // the barriers' phases in step
       const bool warp_dead = __all_sync(kFull, !real);
       // ---- this thread's query row into tensor memory, 16-bit pairs (every MMA of the
       // previous item has completed); rows of no query are zero
@@ -647,64 +766,104 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nsub; ++j, ++g) {
         const int tok0 = t0 + j * SUB, nv = min(SUB, t1 - tok0);  // tokens of the item here
+        const int c0 = NL * hs;  // this stream's first token of the step
         if (in_dec && j + 1 == nsub && stid == 0) cnt_seen = ld_acquire_gpu(&p.unit_cnt[u]);
         if (!T::FP8 && nv < SUB) {
           // the zeroing below writes into the V slot: the tile must have landed (this wait
           // orders the writes after the copy)
-          wait_bar(&full_v[g % T::NSTAGE], (g / T::NSTAGE) & 1);
+          wait_bar(&full_v[g % T::NRING], (g / T::NRING) & 1);
         }
-        wait_bar(&s_full[g % T::NSP], (g / T::NSP) & 1);
+        wait_bar(&s_full[g % NSP], (g / NSP) & 1);
         tc_fence_after();
-        if (g >= (uint32_t)T::NSP) wait_pv_step(g - T::NSP);  // (complete: S(g) came after it)
+        if (g >= (uint32_t)NSP) wait_pv_step(g - NSP);  // (complete: S(g) came after it)
+        const float* sks = reinterpret_cast<const float*>(smem + T::OFF_SC);  // K, then V scales
+        if constexpr (T::TOKS) {
+          sks += (g % T::NSC) * (T::SC_SLOT / 4);
+          wait_bar(&sc_full[g % T::NSC], (g / T::NSC) & 1);
+        }
         if (!warp_dead) {
-          const uint32_t t_sg = t_s + (g % T::NSP) * SUB + lane_off;
-          float x[SUB];
-          tmem_ld64(t_sg, x);
-          // ---- online softmax of this thread's row (log2 units), two logits per instruction
+          const uint32_t t_sg = t_s + (g % NSP) * SUB + lane_off;
+          float x[NL];
+          if constexpr (NL == 64)
+            tmem_ld64(t_sg, x);
+          else
+            tmem_ld32(t_sg + c0, x);
+          // ---- online softmax of this thread's logits (log2 units), two per instruction
           const float2 s2 = make_float2(qk_scale, qk_scale), z2 = make_float2(0.f, 0.f);
+          if constexpr (T::TOKS) {
+            // logit j of the step times its key's scale
 #pragma unroll
-          for (int i = 0; i < SUB / 2; ++i) {
-            const float2 y = ffma2(make_float2(x[2 * i], x[2 * i + 1]), s2, z2);
-            x[2 * i] = y.x;
-            x[2 * i + 1] = y.y;
+            for (int i = 0; i < NL / 4; ++i) {
+              const float4 k4 = *reinterpret_cast<const float4*>(sks + c0 + 4 * i);
+              const float2 a = ffma2(make_float2(x[4 * i], x[4 * i + 1]), s2, z2);
+              const float2 c = ffma2(make_float2(x[4 * i + 2], x[4 * i + 3]), s2, z2);
+              const float2 ya = ffma2(a, make_float2(k4.x, k4.y), z2);
+              const float2 yc = ffma2(c, make_float2(k4.z, k4.w), z2);
+              x[4 * i] = ya.x;
+              x[4 * i + 1] = ya.y;
+              x[4 * i + 2] = yc.x;
+              x[4 * i + 3] = yc.y;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < NL / 2; ++i) {
+              const float2 y = ffma2(make_float2(x[2 * i], x[2 * i + 1]), s2, z2);
+              x[2 * i] = y.x;
+              x[2 * i + 1] = y.y;
+            }
           }
           // masked keys (past the item's tokens or past the row's causal limit) become -inf;
           // most steps have none
-          if (nv < SUB || tok0 + SUB > lim) {
+          if (c0 + NL > nv || tok0 + c0 + NL > lim) {
 #pragma unroll
-            for (int jj = 0; jj < SUB; ++jj)
-              if (jj >= nv || tok0 + jj >= lim) x[jj] = -INFINITY;
+            for (int jj = 0; jj < NL; ++jj)
+              if (c0 + jj >= nv || tok0 + c0 + jj >= lim) x[jj] = -INFINITY;
           }
           float mx = -INFINITY;
 #pragma unroll
-          for (int jj = 0; jj < SUB; jj += 2) mx = fmaxf(mx, fmaxf(x[jj], x[jj + 1]));
+          for (int jj = 0; jj < NL; jj += 2) mx = fmaxf(mx, fmaxf(x[jj], x[jj + 1]));
           const bool need = mx > m_run + 8.f;  // lazy rescale: only when the max grows by 2^8
           const bool rescale = __any_sync(kFull, need);
           const float mn = need ? mx : m_run;
           const float alpha = (mn == m_run || m_run == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
           m_run = mn;
-          // this thread's row of P, 16-bit pairs over the first SUB / 2 columns of its own
-          // logits (all of them are in registers); a masked logit (-inf) gives exp2 = 0, and a
-          // row with no visible key so far has only zeros
+          // this thread's part of its row of P, 16-bit pairs over the first SUB / 2 columns
+          // of its own logits (all of them are in registers); a masked logit (-inf) gives
+          // exp2 = 0, and a row with no visible key so far has only zeros.  With two streams
+          // the other stream's half of the row is written as zeros.
           float lsum = 0.f;
           {
             const float2 nm = make_float2(m_run == -INFINITY ? 0.f : -m_run,
                                           m_run == -INFINITY ? 0.f : -m_run);
             const float2 one2 = make_float2(1.f, 1.f);
             float2 ls2 = z2;
+            const float* svs = sks + T::TT;
 #pragma unroll
-            for (int h = 0; h < SUB / 32; ++h) {  // 32 tokens = 16 columns at a time
+            for (int h = 0; h < NL / 32; ++h) {  // 32 tokens = 16 columns at a time
               uint32_t pk[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const float2 t = ffma2(make_float2(x[32 * h + 2 * i], x[32 * h + 2 * i + 1]), one2, nm);
-                const float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
+                float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
                 ls2 = ffma2(make_float2(p0, p1), one2, ls2);
+                if constexpr (T::TOKS) {
+                  // the value row's scale enters P (a stale scale past the item's tokens meets
+                  // a zero weight and is dropped)
+                  const float2 v2 = *reinterpret_cast<const float2*>(svs + c0 + 32 * h + 2 * i);
+                  p0 = p0 == 0.f ? 0.f : p0 * v2.x;
+                  p1 = p1 == 0.f ? 0.f : p1 * v2.y;
+                }
                 pk[i] = pack16x2<BF>(p0, p1);
               }
-              tmem_st16u(t_sg + 16 * h, pk);
+              tmem_st16u(t_sg + (c0 + 32 * h) / 2, pk);
             }
             lsum = ls2.x + ls2.y;
+            if constexpr (DUAL) {
+              uint32_t zk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) zk[i] = 0u;
+              tmem_st16u(t_sg + (NL - c0) / 2, zk);
+            }
           }
           l_run = l_run * alpha + lsum;
           if (rescale && j > 0) {
@@ -725,7 +884,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         if (!T::FP8 && nv < SUB) {
           // value rows past the item's tokens may hold anything: zero them (before this
           // step's PV reads them) so that zero weights stay zero
-          char* vt = smem + T::OFF_V + (g % T::NSTAGE) * T::SLOT;
+          char* vt = smem + T::OFF_V + (g % T::NRING) * T::SLOT;
           for (int e = stid; e < (SUB - nv) * T::NSLAB * 8; e += 128) {
             const int rr = nv + e / (T::NSLAB * 8), sl = (e / 8) % T::NSLAB, c = e & 7;
             *reinterpret_cast<uint4*>(vt + sl * T::KSLAB + sw128_chunk(rr, c)) =
@@ -735,7 +894,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         fence_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[g % T::NSP]);
+        if (lane == 0) {
+          mbar_arrive(&p_full[g % NSP]);
+          if constexpr (T::TOKS) mbar_arrive(&sc_free[g % T::NSC]);
+        }
       }
       // ---- epilogue: O of this thread's row from tensor memory, in two halves of 64 dims
       wait_pv_step(g - 1);  // every PV of the item (in order)
@@ -743,69 +905,117 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       named_barrier_sync(SOFT_BAR, 128);
       const bool fin = in_dec && slot == uinfo.x && *cnt_seen_s == uinfo.y - 1;
       const size_t orow = ((size_t)b * p.Sq + qi) * p.Hq + hq;
-      float inv = l_run > 0.f ? vts / l_run : 0.f;
-      float lse2 = l_run > 0.f ? m_run + fast_log2(l_run) : -INFINITY;
-      // piece 0 finishing the unit: merged with pieces 1 .. ns-1 in the arithmetic of merge_unit
-      float mx = lse2, wown = 0.f, W = 0.f;
-      if (fin && real) {
-        for (int sp2 = 1; sp2 < uinfo.y; ++sp2)
-          mx = fmaxf(mx, __ldcg(p.lse_part + (size_t)piece_slot(uinfo.x, sp2) * MP + r));
-        wown = lse2 == -INFINITY ? 0.f : fast_exp2(lse2 - mx);
-        W = 0.f + wown;
-      }
-      const bool to_out = slot < 0 || fin;
+      // two streams: the second hands its O row, max and sum to the first through shared
+      // memory, and the first merges them with its own (log-sum-exp rule)
+      float w_own = 1.f, w_oth = 0.f;
+      if constexpr (DUAL) {
+        if (hs == 1) {
 #pragma unroll 1
-      for (int h = 0; h < D / 64; ++h) {
-        float o[64];
-        tmem_ld64(t_o + lane_off + 64 * h, o);
-        if (h == D / 64 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(o_free);  // the next item's first PV may overwrite O
-        }
-        if (!real) continue;
-        float oinv = inv;
-        if (fin) {
+          for (int h = 0; h < D / 64; ++h) {
+            float o[64];
+            tmem_ld64(t_o + lane_off + 64 * h, o);
+            float* row = mrg + qr * D;
 #pragma unroll
-          for (int d = 0; d < 64; ++d) o[d] = wown == 0.f ? 0.f : __fmaf_rn(wown, o[d] * inv, 0.f);
-          float Wh = 0.f + wown;
-          for (int sp2 = 1; sp2 < uinfo.y; ++sp2) {
-            const size_t part = (size_t)piece_slot(uinfo.x, sp2) * MP + r;
-            const float ls = __ldcg(p.lse_part + part);
-            const float ws = ls == -INFINITY ? 0.f : fast_exp2(ls - mx);
-            Wh = Wh + ws;
-            if (ws == 0.f) continue;
-            const float4* op = reinterpret_cast<const float4*>(p.o_part + part * D + 64 * h);
-#pragma unroll
-            for (int d4 = 0; d4 < 16; ++d4) {
-              const float4 w4 = __ldcg(op + d4);
-              o[4 * d4] = __fmaf_rn(ws, w4.x, o[4 * d4]);
-              o[4 * d4 + 1] = __fmaf_rn(ws, w4.y, o[4 * d4 + 1]);
-              o[4 * d4 + 2] = __fmaf_rn(ws, w4.z, o[4 * d4 + 2]);
-              o[4 * d4 + 3] = __fmaf_rn(ws, w4.w, o[4 * d4 + 3]);
+            for (int c = 0; c < 16; ++c) {
+              const int ch = 16 * h + c;  // 16-byte chunk of the row
+              *reinterpret_cast<float4*>(row + 4 * (ch ^ (qr & 7))) =
+                  make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
             }
           }
-          W = Wh;
-          oinv = W > 0.f ? 1.f / W : 0.f;
+          mrg_ml[2 * qr] = m_run;
+          mrg_ml[2 * qr + 1] = l_run;
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free);  // this warp has read its rows of O
         }
-        if (to_out) {
-#pragma unroll
-          for (int d = 0; d < 64; d += 4)
-            store_out4<QK>(p.out, orow * D + 64 * h + d,
-                           make_float4(o[d] * oinv, o[d + 1] * oinv, o[d + 2] * oinv, o[d + 3] * oinv));
-        } else {
-          float4* op = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * MP + r) * D + 64 * h);
-#pragma unroll
-          for (int d = 0; d < 64; d += 4)
-            op[d / 4] = make_float4(o[d] * oinv, o[d + 1] * oinv, o[d + 2] * oinv, o[d + 3] * oinv);
+        named_barrier_sync(SOFT_BAR, 128);  // the second stream's rows are in shared memory
+        if (hs == 0) {
+          const float m2 = mrg_ml[2 * qr], l2 = mrg_ml[2 * qr + 1];
+          const float mm = fmaxf(m_run, m2);
+          w_own = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mm);
+          w_oth = m2 == -INFINITY ? 0.f : fast_exp2(m2 - mm);
+          l_run = l_run * w_own + l2 * w_oth;
+          m_run = mm;
         }
       }
-      if (real) {
-        if (fin) lse2 = W > 0.f ? mx + fast_log2(W) : -INFINITY;
-        if (to_out) {
-          if (p.lse) p.lse[orow] = lse2 * kLn2;
-        } else {
-          p.lse_part[(size_t)slot * MP + r] = lse2;
+      if (!DUAL || hs == 0) {
+        float inv = l_run > 0.f ? vts / l_run : 0.f;
+        float lse2 = l_run > 0.f ? m_run + fast_log2(l_run) : -INFINITY;
+        // piece 0 finishing the unit: merged with pieces 1 .. ns-1 in the arithmetic of
+        // merge_unit
+        float mx = lse2, wown = 0.f, W = 0.f;
+        if (fin && real) {
+          for (int sp2 = 1; sp2 < uinfo.y; ++sp2)
+            mx = fmaxf(mx, __ldcg(p.lse_part + (size_t)piece_slot(uinfo.x, sp2) * MP + qr));
+          wown = lse2 == -INFINITY ? 0.f : fast_exp2(lse2 - mx);
+          W = 0.f + wown;
+        }
+        const bool to_out = slot < 0 || fin;
+#pragma unroll 1
+        for (int h = 0; h < D / 64; ++h) {
+          float o[64];
+          tmem_ld64(t_o + lane_off + 64 * h, o);
+          if (h == D / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);  // the next item's first PV may overwrite O
+          }
+          if (!real) continue;
+          if constexpr (DUAL) {
+            const float* row = mrg + qr * D;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int ch = 16 * h + c;
+              const float4 q4 = *reinterpret_cast<const float4*>(row + 4 * (ch ^ (qr & 7)));
+              o[4 * c] = o[4 * c] * w_own + q4.x * w_oth;
+              o[4 * c + 1] = o[4 * c + 1] * w_own + q4.y * w_oth;
+              o[4 * c + 2] = o[4 * c + 2] * w_own + q4.z * w_oth;
+              o[4 * c + 3] = o[4 * c + 3] * w_own + q4.w * w_oth;
+            }
+          }
+          float oinv = inv;
+          if (fin) {
+#pragma unroll
+            for (int d = 0; d < 64; ++d) o[d] = wown == 0.f ? 0.f : __fmaf_rn(wown, o[d] * inv, 0.f);
+            float Wh = 0.f + wown;
+            for (int sp2 = 1; sp2 < uinfo.y; ++sp2) {
+              const size_t part = (size_t)piece_slot(uinfo.x, sp2) * MP + qr;
+              const float ls = __ldcg(p.lse_part + part);
+              const float ws = ls == -INFINITY ? 0.f : fast_exp2(ls - mx);
+              Wh = Wh + ws;
+              if (ws == 0.f) continue;
+              const float4* op = reinterpret_cast<const float4*>(p.o_part + part * D + 64 * h);
+#pragma unroll
+              for (int d4 = 0; d4 < 16; ++d4) {
+                const float4 w4 = __ldcg(op + d4);
+                o[4 * d4] = __fmaf_rn(ws, w4.x, o[4 * d4]);
+                o[4 * d4 + 1] = __fmaf_rn(ws, w4.y, o[4 * d4 + 1]);
+                o[4 * d4 + 2] = __fmaf_rn(ws, w4.z, o[4 * d4 + 2]);
+                o[4 * d4 + 3] = __fmaf_rn(ws, w4.w, o[4 * d4 + 3]);
+              }
+            }
+            W = Wh;
+            oinv = W > 0.f ? 1.f / W : 0.f;
+          }
+          if (to_out) {
+#pragma unroll
+            for (int d = 0; d < 64; d += 4)
+              store_out4<QK>(p.out, orow * D + 64 * h + d,
+                             make_float4(o[d] * oinv, o[d + 1] * oinv, o[d + 2] * oinv, o[d + 3] * oinv));
+          } else {
+            float4* op = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * MP + qr) * D + 64 * h);
+#pragma unroll
+            for (int d = 0; d < 64; d += 4)
+              op[d / 4] = make_float4(o[d] * oinv, o[d + 1] * oinv, o[d + 2] * oinv, o[d + 3] * oinv);
+          }
+        }
+        if (real) {
+          if (fin) lse2 = W > 0.f ? mx + fast_log2(W) : -INFINITY;
+          if (to_out) {
+            if (p.lse) p.lse[orow] = lse2 * kLn2;
+          } else {
+            p.lse_part[(size_t)slot * MP + qr] = lse2;
+          }
         }
       }
       named_barrier_sync(SOFT_BAR, 128);  // partials written (or the unit finished)
@@ -827,9 +1037,9 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   } else {
     // ================================================================ fp8 widening
     if constexpr (T::FP8) {
-      // step g: the e4m3 K rows of ring slot g % NSTAGE become the f16 rows of K buffer
-      // g % NCK, then its V rows those of V buffer g % NCV (rows past the item's tokens
-      // become zero); the per-tensor scales are applied to the logits and the output
+      // step g: the e4m3 K rows of ring slot g % NRING become the f16 rows of K buffer
+      // g % NSP, then its V rows those of V buffer g % NSP (rows past the item's tokens
+      // become zero); the scales are applied to the logits and P, not here
       const int ctid = tid - T::W_CONV * 32;  // 0 .. 32 NCW - 1
       // one operand: 64 rows of 128 e4m3 codes -> two slabs of 64 rows of 64 f16 values
       auto widen = [&](const char* src, char* dst, int nv) {
@@ -861,30 +1071,29 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         const int nsub = ceil_div(t1 - t0, SUB);
         for (int j = 0; j < nsub; ++j, ++g) {
           const int nv = min(SUB, t1 - (t0 + j * SUB));
-          const int slot = (int)(g % T::NSTAGE);
-          const uint32_t ph = (g / T::NSTAGE) & 1;
-          // ---- K rows
+          const int slot = (int)(g % T::NRING);
+          const uint32_t ph = (g / T::NRING) & 1;
+          // ---- K rows (buffer g % NSP is free once the S of step g - NSP has completed)
           wait_bar(&full_k[slot], ph);
-          if (g >= (uint32_t)T::NCK) {  // the S of step g - NCK has read this buffer
-            const uint32_t x = g - T::NCK;
-            wait_bar(&ck_free[x % T::NCK], (x / T::NCK) & 1);
+          if (g >= (uint32_t)NSP) {
+            const uint32_t x = g - NSP;
+            wait_bar(&s_full[x % NSP], (x / NSP) & 1);
           }
-          widen(smem + T::OFF_K + slot * T::SLOT,
-                smem + T::OFF_CV + (g % T::NCK) * T::CV_BUF, nv);
+          widen(smem + T::OFF_K + slot * T::SLOT, smem + T::OFF_CV + (g % NSP) * T::CV_BUF, nv);
           if (lane == 0) {
-            mbar_arrive(&ck_full[g % T::NCK]);
+            mbar_arrive(&ck_full[g % NSP]);
             mbar_arrive(&empty_k[slot]);  // this warp is done with the K slot
           }
-          // ---- V rows
+          // ---- V rows (buffer g % NSP is free once the PV of step g - NSP has completed)
           wait_bar(&full_v[slot], ph);
-          if (g >= (uint32_t)T::NCV) {  // the PV of step g - NCV has read this buffer
-            const uint32_t x = g - T::NCV;
-            wait_bar(&cv_free[x % T::NCV], (x / T::NCV) & 1);
+          if (g >= (uint32_t)NSP) {
+            const uint32_t x = g - NSP;
+            wait_bar(&pv_done[x % NSP], (x / NSP) & 1);
           }
           widen(smem + T::OFF_V + slot * T::SLOT,
-                smem + T::OFF_CV + (T::NCK + g % T::NCV) * T::CV_BUF, nv);
+                smem + T::OFF_CV + (NSP + g % NSP) * T::CV_BUF, nv);
           if (lane == 0) {
-            mbar_arrive(&cv_full[g % T::NCV]);
+            mbar_arrive(&cv_full[g % NSP]);
             mbar_arrive(&empty_v[slot]);
           }
         }
@@ -912,12 +1121,9 @@ cudaError_t launch_tc_instance(const KernelParams& prm, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, int grid, cudaStream_t s) {
   using T = TcTraits<D, MP, KVK, TOKS>;
   auto kern = decode_tc_kernel<D, MP, KVK, QK, TOKS>;
-  static bool attr_set = false;  // benign race: every caller sets the same value
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};  // devices whose limit is raised
+  const cudaError_t e = set_smem_attr_once(attr_done, reinterpret_cast<const void*>(kern), T::SMEM);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(T::NTHREADS);

@@ -313,13 +313,10 @@ extern "C" pa_status pa_gather_kv(const pa_config* cfg, const void* k_cache, con
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PA_ERR_CUDA;
   const size_t smem = gather_smem_bytes(c.batch);
-  static bool attr_set = false;  // benign race: every caller sets the same value
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)gather_smem_bytes(kGatherMaxBatch)) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};  // devices whose limit is raised
+  if (set_smem_attr_once(attr_done, reinterpret_cast<const void*>(gather_kernel),
+                         (int)gather_smem_bytes(kGatherMaxBatch)) != cudaSuccess)
+    return PA_ERR_CUDA;
   gather_kernel<<<sms, kGatherThreads, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

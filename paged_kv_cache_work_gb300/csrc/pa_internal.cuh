@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pa.h"
 
 namespace pa {
@@ -84,21 +86,19 @@ constexpr int kTcMinRows = 33;
 
 // Everything but the grid size, which needs the device (see api.cu).
 // Every cache whose tile row is at least one 128-byte slab runs on tensor cores: a 16-bit
-// cache with head dim 128 or 256, or an fp8 cache with head dim 128 and per-tensor or no
-// scales, and more than 32 query rows per kv head on tcgen05 (row tiles of 64 or 128, the
-// MMA always 128 rows), otherwise on mma.sync with the rows padded to 16, 32 or 64 (larger
-// groups cut into 64-row tiles): even a tile of one real row in sixteen costs less there
-// than CUDA-core arithmetic.  (Per-token fp8 scales measured faster on mma.sync, which
-// applies them in registers.)  A 64-dim fp8 cache (64-byte rows) runs on the CUDA-core
-// kernel, in tiles of up to 8 rows.
+// cache with head dim 128 or 256, or an fp8 cache with head dim 128 (any scale mode), and
+// more than 32 query rows per kv head on tcgen05 (row tiles of 64 or 128, the MMA always
+// 128 rows), otherwise on mma.sync with the rows padded to 16, 32 or 64 (larger groups cut
+// into 64-row tiles): even a tile of one real row in sixteen costs less there than
+// CUDA-core arithmetic.  A 64-dim fp8 cache (64-byte rows) runs on the CUDA-core kernel, in
+// tiles of up to 8 rows.
 inline Variant make_variant(const pa_config& c) {
   Variant v{};
   v.rows = (c.num_q_heads / c.num_kv_heads) * c.max_q_len;
   v.bpe = c.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
   v.path = c.head_dim * v.bpe >= 128 ? 1 : 0;
   if (v.path == 1 && c.head_dim >= 128 && v.rows >= kTcMinRows &&
-      (c.kv_dtype != PA_FP8_E4M3 ||
-       (c.head_dim == 128 && c.kv_scale_mode != PA_SCALE_PER_TOKEN)))
+      (c.kv_dtype != PA_FP8_E4M3 || c.head_dim == 128))
     v.path = 2;
   if (v.path == 2)
     v.mp = v.rows <= 64 ? 64 : 128;
@@ -195,6 +195,21 @@ __host__ __device__ constexpr int ilog2(uint32_t x) { return x <= 1 ? 0 : 1 + il
 // Partial slot of piece s of a unit whose first piece sits in slot `first`.
 __host__ __device__ inline int piece_slot(int first, int s) {
   return s == 0 ? first : 2 * ((first >> 1) + s);
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device, once per
+// device: the attribute belongs to the device, so a process that launches on several GPUs
+// sets it on each.  `done` is the caller's per-kernel bit set of devices already set up
+// (devices past the 64th are set up on every launch).
+inline cudaError_t set_smem_attr_once(std::atomic<uint64_t>& done, const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 // Launch helpers implemented in plan.cu / decode_*.cu / reduce.cu.
@@ -317,6 +332,17 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Untiled bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// global into shared memory, completing on `bar` (tx bytes).
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
 

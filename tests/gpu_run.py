@@ -84,8 +84,7 @@ def decode_merge_limit(split_merge: int) -> int:
 def variant(cfg: pa.PaConfig, ctas: int):
     rows = (cfg.num_q_heads // cfg.num_kv_heads) * cfg.max_q_len
     bpe = 1 if cfg.kv_dtype == pa.FP8_E4M3 else 2
-    tc = cfg.head_dim >= 128 and rows >= TC_MIN_ROWS and (
-        bpe == 2 or (cfg.head_dim == 128 and cfg.kv_scale_mode != pa.SCALE_PER_TOKEN))
+    tc = cfg.head_dim >= 128 and rows >= TC_MIN_ROWS and (bpe == 2 or cfg.head_dim == 128)
     if tc:  # tcgen05
         mp = 64 if rows <= 64 else 128
     elif cfg.head_dim * bpe >= 128:  # mma.sync kernel

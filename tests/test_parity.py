@@ -145,14 +145,15 @@ EDGE = [
     ("mma_fp8_fp16q_rows32", dict(batch=2, max_q_len=2, num_q_heads=16, num_kv_heads=1,
                                   head_dim=128, block_size=16, ctx=[99, 180], q_dtype="fp16",
                                   kv_dtype="fp8", scale_mode="none")),
-    # per-token fp8 scales stay on mma.sync at every row count
-    ("mma_fp8_token_fp16q_rows64", dict(batch=3, max_q_len=4, num_q_heads=16, num_kv_heads=1,
+    # per-token fp8 scales on mma.sync (up to 32 rows per kv head)
+    ("mma_fp8_token_fp16q_rows32", dict(batch=3, max_q_len=2, num_q_heads=16, num_kv_heads=1,
                                         head_dim=128, block_size=16, ctx=[129, 70, 640],
                                         q_dtype="fp16", kv_dtype="fp8", scale_mode="token",
                                         causal=True)),
-    ("mma_fp8_token_rows100", dict(batch=2, max_q_len=4, num_q_heads=25, num_kv_heads=1,
-                                   head_dim=128, block_size=1024, ctx=[1500, 2049],
-                                   kv_dtype="fp8", scale_mode="token", causal=True)),
+    ("mma_fp8_token_rows16_long_pages", dict(batch=2, max_q_len=1, num_q_heads=16,
+                                             num_kv_heads=1, head_dim=128, block_size=1024,
+                                             ctx=[1500, 2049], kv_dtype="fp8",
+                                             scale_mode="token", causal=True)),
     ("mma_d64_fp8_stays_on_cuda_cores", dict(batch=2, max_q_len=1, num_q_heads=16,
                                              num_kv_heads=1, head_dim=64, block_size=16,
                                              ctx=[70, 130], kv_dtype="fp8", scale_mode="token")),
@@ -171,9 +172,25 @@ def test_edge_cases(name, kw, cuda_device, pa):
 
 
 # The tcgen05 kernel: 16-bit caches with head dim 128 or 256 and fp8 caches with head dim 128
-# and per-tensor or no scales, more than 32 query rows per kv head (tiles of 64 or 128 rows,
-# MMA always 128 rows).
+# (per-tensor, per-token or no scales), more than 32 query rows per kv head (tiles of 64 or
+# 128 rows, MMA always 128 rows; 64-row tiles of head dim 128 run as two token streams).
 TC = [
+    ("fp8_token_fp16q_rows64", dict(batch=3, max_q_len=4, num_q_heads=16, num_kv_heads=1,
+                                    block_size=16, ctx=[129, 70, 640], q_dtype="fp16",
+                                    kv_dtype="fp8", scale_mode="token", causal=True)),
+    ("fp8_token_rows100_tile128", dict(batch=2, max_q_len=4, num_q_heads=25, num_kv_heads=1,
+                                       block_size=1024, ctx=[1500, 2049], kv_dtype="fp8",
+                                       scale_mode="token", causal=True)),
+    ("fp8_token_rows40_partial", dict(batch=3, max_q_len=5, num_q_heads=8, num_kv_heads=1,
+                                      block_size=32, ctx=[5, 191, 64], kv_dtype="fp8",
+                                      scale_mode="token", causal=True)),
+    ("fp8_token_two_kv_heads_ragged", dict(batch=4, max_q_len=4, num_q_heads=32,
+                                           num_kv_heads=2, block_size=64, ctx=[0, 4, 300, 65],
+                                           q_lens=[0, 4, 1, 3], kv_dtype="fp8",
+                                           scale_mode="token", causal=True)),
+    ("fp8_token_long_pages_not_causal", dict(batch=2, max_q_len=4, num_q_heads=16,
+                                             num_kv_heads=1, block_size=1024, ctx=[3000, 1025],
+                                             kv_dtype="fp8", scale_mode="token")),
     ("rows33_padded_causal", dict(batch=3, max_q_len=3, num_q_heads=11, num_kv_heads=1,
                                   block_size=16, ctx=[70, 300, 129], causal=True)),
     ("rows64_long_pages", dict(batch=2, max_q_len=4, num_q_heads=16, num_kv_heads=1,
