@@ -111,8 +111,8 @@ FULL = {w.name: w for w in [TINY_CTX128, TINY_CTX512, GQA_B32, LONG_SQ1, LONG_SQ
                             FP8_TENSOR_SQ1, FP8_TENSOR_SQ4, FP8_TOKEN_SQ1, FP8_TOKEN_SQ4,
                             *MHA_D256]}
 
-# The batched-GQA problem is the throughput workload the bench times.
-BENCH = GQA_B32
+# The largest problem that fits one GPU (about 4.7 GB of KV): the bench's headline workload.
+BENCH = FULL["mha_b32_h16_kv16_d256_bs32_sq64"]
 
 
 def reduced(w: Workload, batch: int, ctx_lo: int, ctx_hi: int) -> Workload:
