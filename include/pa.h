@@ -42,9 +42,10 @@
  * context_lens, q_lens, out, lse and ws.  q, k_cache, v_cache and out must be
  * 16-byte aligned; ws 256-byte aligned.
  *
- * Besides the step, pa_gather_kv copies a batch's cached K and V rows out of the
- * pages into contiguous buffers (the workspace copy of the HSTU paged attention),
- * with the same calling convention.
+ * Besides the step, pa_append_kv writes a step's new K/V rows into their pages
+ * (quantising them to fp8 where the cache is fp8), and pa_gather_kv copies a batch's
+ * cached K and V rows out of the pages into contiguous buffers (the workspace copy of
+ * the HSTU paged attention), with the same calling convention.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -180,6 +181,9 @@ PA_API pa_status pa_read_flags(const void *ws, size_t ws_bytes, int32_t *flags, 
  * every GPU where the library's device code is loaded and held until the process exits.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current and caches it; make that first call before any stream capture.
+ * The cached address belongs to the device's primary context: after cudaDeviceReset (or any
+ * other teardown of that context) it names freed memory, so a process that resets a device
+ * must not call this entry point on that device again.
  * A problem whose pa_workspace_size() exceeds PA_STATIC_SCRATCH_BYTES is rejected with
  * PA_ERR_WORKSPACE before anything is launched.  All calls on a device share the one array
  * and each call overwrites what the previous one left there: calls whose kernels overlap on
@@ -224,6 +228,44 @@ PA_API pa_status pa_gather_kv(const pa_config *cfg, const void *k_cache, const v
                               const int32_t *block_tables, const int32_t *context_lens,
                               void *k_out, void *v_out, int64_t max_rows, int32_t *row_offsets,
                               int32_t *flags, pa_stream stream);
+
+/* Quantise-on-write KV append: write a decode step's new K/V rows into their pages.
+ *
+ * New row i < q_lens[b] of sequence b is cache position pos = context_lens[b] - q_lens[b] + i
+ * (the new tokens are the last q_lens[b] of the context_lens[b] tokens, the positions the
+ * decode's causal mask gives them), i.e. slot pos % block_size of physical block
+ * block_tables[b][pos / block_size] ("HSTU Paged Attention", RecSDK issue 1281, background:
+ * the paged KV cache).  Call it before pa_plan / pa_decode with the same tables and lengths.
+ *   16-bit cache (kv_dtype == q_dtype): the row's bits are copied unchanged.
+ *   fp8 cache: OCP E4M3 codes of row / scale, rounded to nearest (ties to even), magnitudes
+ *   past 448 saturating to 448; scale modes of "Optimize paged-attention metadata decode"
+ *   (FlyDSL PR #910, Breaking Changes: per_token_kv):
+ *     PA_SCALE_PER_TOKEN   scale = amax(|row|) / 448 (1 for an all-zero row), computed in fp32
+ *                          and WRITTEN to k_scale / v_scale [num_blocks, block_size, Hkv];
+ *     PA_SCALE_PER_TENSOR  scale = k_scale[0] / v_scale[0], READ (one fp32 each);
+ *     PA_SCALE_NONE        scale 1; k_scale / v_scale may be NULL.
+ *   Quotients are IEEE fp32 divisions.  A NaN element gives a NaN code (0x7f or 0xff).
+ * Reads cfg's batch, max_q_len, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+ * num_blocks, q_dtype, kv_dtype and kv_scale_mode.
+ *
+ *   k_new, v_new   device, [batch, max_q_len, num_kv_heads, head_dim] in q_dtype, 16-byte
+ *                  aligned; rows i >= q_lens[b] are ignored
+ *   block_tables, context_lens, q_lens   device int32, as for pa_plan
+ *   k_cache, v_cache   device, [num_blocks, block_size, num_kv_heads, head_dim] in kv_dtype,
+ *                  16-byte aligned; only the new rows' slots are written
+ *   k_scale, v_scale   device fp32 (see the scale modes)
+ *   flags          NULL, or a device int32 the call ORs PA_FLAG_* bits into:
+ *                  PA_FLAG_BAD_LENGTHS for a sequence whose lengths break the rules of
+ *                  pa_plan (none of its rows is written), PA_FLAG_BAD_BLOCK_ID for a new row
+ *                  whose page lies outside [0, num_blocks) (that row is not written)
+ *
+ * Stream-ordered, allocates nothing, never synchronises.  PA_ERR_INVALID_ARG for NULL or
+ * misaligned pointers (scales NULL with a scale mode), PA_ERR_UNSUPPORTED for head_dim,
+ * block_size or dtype combinations the decode does not take. */
+PA_API pa_status pa_append_kv(const pa_config *cfg, const void *k_new, const void *v_new,
+                              const int32_t *block_tables, const int32_t *context_lens,
+                              const int32_t *q_lens, void *k_cache, void *v_cache,
+                              float *k_scale, float *v_scale, int32_t *flags, pa_stream stream);
 
 /* A static, human-readable name of a status. */
 PA_API const char *pa_status_string(pa_status status);

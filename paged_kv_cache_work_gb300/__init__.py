@@ -15,7 +15,7 @@ import os
 from typing import Optional
 
 __all__ = ["PaConfig", "PaError", "load", "workspace_size", "plan", "decode", "reduce",
-           "decode_step_static", "STATIC_SCRATCH_BYTES",
+           "decode_step_static", "STATIC_SCRATCH_BYTES", "append_kv", "gather_kv",
            "read_flags", "status_string", "config_for", "paged_attention", "LIB_PATH",
            "BF16", "FP16", "FP8_E4M3", "SCALE_NONE", "SCALE_PER_TENSOR", "SCALE_PER_TOKEN",
            "FLAG_BAD_LENGTHS", "FLAG_BAD_BLOCK_ID", "FLAG_WAIT_TIMEOUT", "EXPORTED_SYMBOLS",
@@ -33,7 +33,7 @@ FLAG_BAD_LENGTHS, FLAG_BAD_BLOCK_ID, FLAG_WAIT_TIMEOUT = 1, 2, 4
 MERGE_AUTO, MERGE_IN_DECODE, MERGE_IN_REDUCE = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("pa_workspace_size", "pa_plan", "pa_decode", "pa_reduce", "pa_read_flags",
-                    "pa_status_string", "pa_decode_step_static", "pa_gather_kv")
+                    "pa_status_string", "pa_decode_step_static", "pa_gather_kv", "pa_append_kv")
 
 # Bytes of the device array behind pa_decode_step_static (PA_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -78,6 +78,8 @@ def load(path: str = LIB_PATH):
     L.pa_decode_step_static.restype = ctypes.c_int
     L.pa_gather_kv.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp]
     L.pa_gather_kv.restype = ctypes.c_int
+    L.pa_append_kv.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.pa_append_kv.restype = ctypes.c_int
     L.pa_status_string.argtypes = [ctypes.c_int]
     L.pa_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -164,6 +166,17 @@ def gather_kv(cfg: PaConfig, k_cache, v_cache, block_tables, context_lens, k_out
     _check("pa_gather_kv", load().pa_gather_kv(
         ctypes.byref(cfg), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         _ptr(k_out), _ptr(v_out), int(max_rows), _ptr(row_offsets), _ptr(flags),
+        _stream(stream)))
+
+
+def append_kv(cfg: PaConfig, k_new, v_new, block_tables, context_lens, q_lens, k_cache, v_cache,
+              k_scale=None, v_scale=None, flags=None, stream=None):
+    """Write a step's new K/V rows into their pages, quantised to fp8 for an fp8 cache (see
+    pa_append_kv in pa.h): new row i of sequence b lands at position
+    context_lens[b] - q_lens[b] + i.  Per-token scales are written into k_scale / v_scale."""
+    _check("pa_append_kv", load().pa_append_kv(
+        ctypes.byref(cfg), _ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(context_lens),
+        _ptr(q_lens), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(flags),
         _stream(stream)))
 
 
