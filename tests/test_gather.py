@@ -151,3 +151,27 @@ def test_gather_copies_nothing_when_the_rows_do_not_fit(cuda_device, pa):
     assert int(flags.item()) & pa.FLAG_BAD_LENGTHS
     assert (_bits(k_out) == 0x5555).all() and (_bits(v_out) == 0x5555).all()
     assert np.array_equal(offs.cpu().numpy(), off.astype(np.int32))  # offsets still written
+
+
+@pytest.mark.gpu
+def test_gather_bad_lengths_count_as_empty_sequences(cuda_device, pa):
+    """A negative length, or one beyond max_blocks_per_seq * block_size, is flagged and that
+    sequence counts as empty: it gets no rows, the offsets stay consistent, and every other
+    sequence is copied bit for bit."""
+    wl = W.reduced(W.GQA_B32, 4, 20, 60)
+    inp = W.make_inputs(wl, W.SEEDS[1], context_lens=[40, 17, 33, 5], q_lens=[1, 1, 1, 1])
+    cap = inp["block_tables"].shape[1] * wl.block_size
+    lens = [-3, 17, cap + 1, 5]
+    ref_inp = dict(inp, context_lens=torch.tensor([0, 17, 0, 5], dtype=torch.int32))
+    k_ref, v_ref, off = oracle.gather_kv(ref_inp)
+    bad = dict(inp, context_lens=torch.tensor(lens, dtype=torch.int32))
+    dev_inp = W.to_device(bad, cuda_device)
+    cfg = pa.config_for(dev_inp, num_ctas=1)
+    flags = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    total = int(off[-1])
+    k_out, v_out, offs = _run_gather(pa, dev_inp, cfg, total + 4, flags)
+    assert int(flags.item()) & pa.FLAG_BAD_LENGTHS
+    assert list(offs.cpu().numpy()) == [0, 0, 17, 17, 22] == list(off.astype(np.int32))
+    assert np.array_equal(_bits(k_out)[:total], k_ref)
+    assert np.array_equal(_bits(v_out)[:total], v_ref)
+    assert (_bits(k_out)[total:] == _sentinel(k_out)).all()

@@ -2,8 +2,9 @@
 (a plugin or framework interface without an allocator, a serving loop that must not call
 cudaMalloc after start-up, or code under stream capture).  It keeps its scratch in a
 static device array inside the library.  Checked here (GPU) through the C ABI against the
-workspace-based entry points, within the parity tolerances, on two calls in a row; and a
-problem too large for the static array is refused before anything runs.
+workspace-based entry points and against the CPU oracle, within the parity tolerances, on
+two calls in a row; and a problem too large for the static array is refused before anything
+runs.
 
 This file is collected last on purpose: the entry point's first call on a device looks the
 array up, and the test must pass both alone in a fresh process and after every other test.
@@ -13,6 +14,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_work_gb300 as pa
 import workloads as W
 from gpu_run import compare
@@ -45,6 +47,7 @@ def test_static_step_matches_workspace_step_twice(wl, cuda_device):
     torch.cuda.synchronize()
     ref_out = ref_out.float().cpu().numpy()
     ref_lse = ref_lse.cpu().numpy()
+    orc_out, orc_lse = oracle.decode(W.to_device(inp, "cpu"), "f32")
     for _ in range(2):
         out = torch.full_like(inp["q"], float("nan"))
         lse = torch.full(inp["q"].shape[:3], float("nan"), dtype=torch.float32,
@@ -52,6 +55,7 @@ def test_static_step_matches_workspace_step_twice(wl, cuda_device):
         assert _static_call(lib, cfg, inp, out, lse) == pa.OK
         torch.cuda.synchronize()
         compare(out, lse, ref_out, ref_lse, wl.kv_dtype)
+        compare(out, lse, orc_out, orc_lse, wl.kv_dtype)
 
 
 def test_static_step_refuses_problems_beyond_its_scratch(cuda_device):
