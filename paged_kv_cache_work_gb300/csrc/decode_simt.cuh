@@ -497,10 +497,10 @@ cudaError_t launch_simt_instance(const KernelParams& prm, const CUtensorMap& kma
   return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, prm);
 }
 
-// Dispatch over the row tile and the dtype combination for one head dimension.
+// Dispatch over the row tile and the dtype combination for one head dimension.  Only caches
+// whose rows are shorter than one 128-byte slab come here (64-dim fp8: every 16-bit cache
+// and every other fp8 cache runs on tensor cores), so only fp8 instances are built.
 #define PA_SIMT_ROWS(X, MP_)        \
-  X(MP_, KV_BF16, Q_BF16, false)    \
-  X(MP_, KV_FP16, Q_FP16, false)    \
   X(MP_, KV_FP8, Q_BF16, false)     \
   X(MP_, KV_FP8, Q_BF16, true)      \
   X(MP_, KV_FP8, Q_FP16, false)     \

@@ -66,23 +66,31 @@ struct TcTraits {
   // released by the commit of the S (K) or the PV (V) of step g that the softmax and the MMA
   // thread wait for anyway.  Head dim 256: three slots (two S/P buffers fit in tensor
   // memory, two slots would leave too little in flight), released by commits of their own.
-  // fp8: three slots of codes, released by the widening warps.
-  static constexpr int NRING = FP8 ? 3 : (D == 256 ? 3 : NSP);
-  static constexpr bool RING_BY_MMA = !FP8 && NRING == NSP;
+  // fp8: three slots of codes, released by the widening warps (deeper fp8 rings, five slots
+  // or two K / seven V, measured no faster: the widening and the MMA set the pace).
+  static constexpr int NK = FP8 ? 3 : (D == 256 ? 3 : NSP);  // K ring slots
+  static constexpr int NV = FP8 ? 3 : (D == 256 ? 3 : NSP);  // V ring slots
+  static constexpr bool K_BY_S = !FP8 && NK == NSP;   // a K slot is released by its S's commit
+  static constexpr bool V_BY_PV = !FP8 && NV == NSP;  // a V slot is released by its PV's commit
   static constexpr int ROWB = 128;             // swizzled slabs of 128 bytes per row
   static constexpr int NSLAB = D * BPE / 128;  // slabs of a cache tile row
   static constexpr int OFF_K = 0;                      // K ring
-  static constexpr int OFF_V = OFF_K + NRING * SLOT;   // V ring
-  // fp8: the widened (f16) K and V rows of NSP steps each, 128-byte-swizzled operands of two
-  // 64-dim slabs; the K buffer of step g is released by its S, the V buffer by its PV
-  static constexpr int NCB = FP8 ? NSP : 0;
+  static constexpr int OFF_V = OFF_K + NK * SLOT;      // V ring
+  // fp8: the widened (f16) K rows of NCK steps and V rows of NCV steps, 128-byte-swizzled
+  // operands of two 64-dim slabs.  Both are indexed by the step modulo NSP, so the K buffer
+  // of step g is released by the S's commit to s_full and the V buffer by the PV's commit to
+  // pv_done (with fewer K buffers they would need a commit of their own, which measured
+  // slower: a commit costs the tensor pipe about 90 clocks).
+  static constexpr int NCK = FP8 ? NSP : 0;
+  static constexpr int NCV = FP8 ? NSP : 0;
+  static constexpr bool CK_BY_S = NCK == NSP;
   static constexpr int CV_SLAB = SUB * 128;
   static constexpr int CV_BUF = 2 * CV_SLAB;
-  static constexpr int OFF_CV = OFF_V + NRING * SLOT;  // K buffers, then V buffers
+  static constexpr int OFF_CV = OFF_V + NV * SLOT;     // K buffers, then V buffers
   static constexpr int SCRATCH = OFF_CV;  // bytes free for the merges at the end (the rings)
   static constexpr int KSLAB = FP8 ? CV_SLAB : TT * 128;  // slab stride of the MMA operands
   // two-stream merge: the second stream's O rows (fp32, 16-byte chunks swizzled by row)
-  static constexpr int OFF_MRG = OFF_CV + 2 * NCB * CV_BUF;
+  static constexpr int OFF_MRG = OFF_CV + (NCK + NCV) * CV_BUF;
   static constexpr int MRG_BYTES = DUAL ? 64 * D * 4 : 0;
   // per-token scales: NSC slots of 64 K then 64 V fp32 scales
   static constexpr int NSC = TOKS ? 8 : 0;
@@ -91,9 +99,10 @@ struct TcTraits {
   static constexpr int OFF_ML = OFF_SC + NSC * SC_SLOT;
   static constexpr int ML_BYTES = round_up(2 * MP * 4 + (DUAL ? 2 * 64 * 4 : 0), 128);
   static constexpr int OFF_BAR = round_up(OFF_ML + ML_BYTES, 64);
-  // full_k, empty_k, full_v, empty_v (NRING each), s_full, p_full, pv_done (NSP each),
-  // o_free, q_full, mma_end, ck_full and cv_full (NCB each), sc_full and sc_free (NSC each)
-  static constexpr int NBAR = 4 * NRING + 3 * NSP + 3 + 2 * NCB + 2 * NSC;
+  // full_k, empty_k (NK each), full_v, empty_v (NV each), s_full, p_full, pv_done (NSP each),
+  // o_free, q_full, mma_end, ck_full and ck_free (NCK each), cv_full (NCV), sc_full and
+  // sc_free (NSC each)
+  static constexpr int NBAR = 2 * NK + 2 * NV + 3 * NSP + 3 + 2 * NCK + NCV + 2 * NSC;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 16 + 1024;
   static constexpr int CTAS_PER_SM = 1;
   // Tensor memory (lane = query row, 32-bit columns): NSP S/P buffers of SUB fp32 columns
@@ -112,6 +121,8 @@ struct TcTraits {
   // g - NSP + LAG, which waits for the K rows of that step: the widening, K(g) then V(g),
   // must not need K rows past g
   static_assert(LAG >= 1 && LAG < NSP, "no cycle between the roles");
+  static_assert(!FP8 || NCK >= 2, "the widening of K(g) waits only for the S of step g - NCK");
+  static_assert(!FP8 || NCV == NSP, "a widened V buffer is released through pv_done");
   static_assert(MP == 64 || MP == 128, "row tile");
   static_assert(D == 128 || D == 256, "head dim");
   static_assert(SUB == 64, "step");
@@ -279,10 +290,10 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
 }
 // The TMA side of the tcgen05 kernel, run by warp 0 (all lanes, same state).  Tile n of the
-// CTA's work list goes to slot n % NRING of the K ring and of the V ring; lane
+// CTA's work list goes to slot n % NK of the K ring and n % NV of the V ring; lane
 // page * NSLAB + slab copies one 128-byte column slab of one page of the tile.  The order of
-// the copies is K(0), K(1), V(0), K(2), V(1), ...: a copy waits until the tile NRING
-// earlier has been read from its slot (by its S for K and its PV for V, or, for fp8, by the
+// the copies is K(0), K(1), V(0), K(2), V(1), ...: a copy waits until the tile one ring
+// length earlier has been read from its slot (by its S for K and its PV for V, or, for fp8, by the
 // widening warps).  Per-token scales of tile n go to slot n % NSC of the scale ring, which
 // the softmax releases.
 //
@@ -410,12 +421,13 @@ struct TcProducer {
     return false;
   }
 
-  // Copy a tile's boxes into slot n % NRING of one ring once the slot is released (the
-  // release barrier completes once per use of the slot, in tile order).
+  // Copy a tile's boxes into slot n % NS of one ring once the slot is released (the release
+  // barrier completes once per use of the slot, in tile order).
+  template <int NS>
   __device__ __forceinline__ bool issue(const Box& bx, uint32_t n, uint64_t* full,
                                         uint64_t* rel, const CUtensorMap* map, int ring) {
-    const int s = (int)(n % T::NRING);
-    if (!wait_or_abort(&rel[s], ((n / T::NRING) & 1) ^ 1)) return false;
+    const int s = (int)(n % NS);
+    if (!wait_or_abort(&rel[s], ((n / NS) & 1) ^ 1)) return false;
     if (lane == 0) mbar_arrive_expect_tx(&full[s], bx.nvalid * box_bytes);
     __syncwarp();
     char* slot = smem + ring + s * T::SLOT;
@@ -472,7 +484,7 @@ struct TcProducer {
 
   // K (and the scales) of a tile, counted as soon as each copy is in flight
   __device__ __forceinline__ bool issue_k(const Box& bx) {
-    if (!issue(bx, nk, full_k, rel_k, kmap, T::OFF_K)) return false;
+    if (!issue<T::NK>(bx, nk, full_k, rel_k, kmap, T::OFF_K)) return false;
     ++nk;
     if (!issue_scales(bx, nsc)) return false;
     ++nsc;
@@ -486,7 +498,7 @@ struct TcProducer {
     while (true) {
       const bool more = next_tile(nxt);
       if (more && !issue_k(nxt)) return;
-      if (!issue(cur, nv, full_v, rel_v, vmap, T::OFF_V)) return;
+      if (!issue<T::NV>(cur, nv, full_v, rel_v, vmap, T::OFF_V)) return;
       ++nv;
       if (!more) return;
       cur = nxt;
@@ -500,10 +512,10 @@ struct TcProducer {
       for (uint32_t j = nsc > (uint32_t)T::NSC ? nsc - T::NSC : 0; j < nsc; ++j)
         mbar_wait_drain(&sc_full[j % T::NSC], (j / T::NSC) & 1);
     }
-    for (uint32_t j = nk > (uint32_t)T::NRING ? nk - T::NRING : 0; j < nk; ++j)
-      mbar_wait_drain(&full_k[j % T::NRING], (j / T::NRING) & 1);
-    for (uint32_t j = nv > (uint32_t)T::NRING ? nv - T::NRING : 0; j < nv; ++j)
-      mbar_wait_drain(&full_v[j % T::NRING], (j / T::NRING) & 1);
+    for (uint32_t j = nk > (uint32_t)T::NK ? nk - T::NK : 0; j < nk; ++j)
+      mbar_wait_drain(&full_k[j % T::NK], (j / T::NK) & 1);
+    for (uint32_t j = nv > (uint32_t)T::NV ? nv - T::NV : 0; j < nv; ++j)
+      mbar_wait_drain(&full_v[j % T::NV], (j / T::NV) & 1);
   }
 };
 
@@ -522,18 +534,19 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   extern __shared__ char smem_raw[];
   char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint64_t* full_k = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
-  uint64_t* empty_k = full_k + T::NRING;
-  uint64_t* full_v = empty_k + T::NRING;
-  uint64_t* empty_v = full_v + T::NRING;
-  uint64_t* s_full = empty_v + T::NRING;  // [NSP]: S of the step in buffer b is complete
+  uint64_t* empty_k = full_k + T::NK;
+  uint64_t* full_v = empty_k + T::NK;
+  uint64_t* empty_v = full_v + T::NV;
+  uint64_t* s_full = empty_v + T::NV;  // [NSP]: S of the step in buffer b is complete
   uint64_t* p_full = s_full + NSP;        // [NSP]: P of the step in buffer b is written
   uint64_t* pv_done = p_full + NSP;       // [NSP]: the PV that read buffer b has completed
   uint64_t* o_free = pv_done + NSP;
   uint64_t* q_full = o_free + 1;
   uint64_t* mma_end = q_full + 1;
-  uint64_t* ck_full = mma_end + 1;       // [NCB]: widened K rows of the step in buffer b
-  uint64_t* cv_full = ck_full + T::NCB;  // [NCB]: widened V rows of the step in buffer b
-  uint64_t* sc_full = cv_full + T::NCB;  // [NSC]: per-token scales of the step in slot b
+  uint64_t* ck_full = mma_end + 1;       // [NCK]: widened K rows of the step in buffer b
+  uint64_t* ck_free = ck_full + T::NCK;  // [NCK]: the S that read buffer b has completed
+  uint64_t* cv_full = ck_free + T::NCK;  // [NCV]: widened V rows of the step in buffer b
+  uint64_t* sc_full = cv_full + T::NCV;  // [NSC]: per-token scales of the step in slot b
   uint64_t* sc_free = sc_full + T::NSC;  // [NSC]: the softmax is done with slot b
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sc_free + T::NSC);
   volatile int* pend = abort_flag + 2;        // [4]: split pieces published, see finish_pending
@@ -543,18 +556,22 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < T::NRING; ++s) {
-      mbar_init(&full_k[s], 1);  // the expect_tx arrival of the copy
-      mbar_init(&full_v[s], 1);
-      // readers of a ring slot: the widening warps (fp8), or the commit of the S (K) or PV
-      // (V) that read it when the ring is not released through s_full / pv_done
+    // readers of a ring slot: the widening warps (fp8), or the commit of the S (K) or PV
+    // (V) that read it when the ring is not released through s_full / pv_done; full: the
+    // expect_tx arrival of the copy
+    for (int s = 0; s < T::NK; ++s) {
+      mbar_init(&full_k[s], 1);
       mbar_init(&empty_k[s], T::FP8 ? T::NCW : 1);
+    }
+    for (int s = 0; s < T::NV; ++s) {
+      mbar_init(&full_v[s], 1);
       mbar_init(&empty_v[s], T::FP8 ? T::NCW : 1);
     }
-    for (int b = 0; b < T::NCB; ++b) {
+    for (int b = 0; b < T::NCK; ++b) {
       mbar_init(&ck_full[b], T::NCW);
-      mbar_init(&cv_full[b], T::NCW);
+      mbar_init(&ck_free[b], 1);
     }
+    for (int b = 0; b < T::NCV; ++b) mbar_init(&cv_full[b], T::NCW);
     for (int b = 0; b < NSP; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 4);
@@ -603,8 +620,8 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   if (warp == T::W_PROD) {
     // ================================================================ TMA producer
     TcProducer<T> prod;
-    prod.init(&p, &kmap, &vmap, smem, full_k, T::RING_BY_MMA ? s_full : empty_k, full_v,
-              T::RING_BY_MMA ? pv_done : empty_v, sc_full, sc_free, abort_flag, lane, it_begin,
+    prod.init(&p, &kmap, &vmap, smem, full_k, T::K_BY_S ? s_full : empty_k, full_v,
+              T::V_BY_PV ? pv_done : empty_v, sc_full, sc_free, abort_flag, lane, it_begin,
               it_end);
     prod.run();  // every tile of the work list, as slots come free
     prod.drain();
@@ -621,10 +638,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         uint32_t vaddr;
         if constexpr (T::FP8) {
           wait_bar(&cv_full[gp % NSP], (gp / NSP) & 1);
-          vaddr = smem_addr(smem + T::OFF_CV + (NSP + gp % NSP) * T::CV_BUF);
+          vaddr = smem_addr(smem + T::OFF_CV + (T::NCK + gp % NSP) * T::CV_BUF);
         } else {
-          const int slot = (int)(gp % T::NRING);
-          wait_bar(&full_v[slot], (gp / T::NRING) & 1);
+          const int slot = (int)(gp % T::NV);
+          wait_bar(&full_v[slot], (gp / T::NV) & 1);
           vaddr = smem_addr(smem + T::OFF_V + slot * T::SLOT);
         }
         wait_bar(&p_full[gp % NSP], (gp / NSP) & 1);
@@ -639,7 +656,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
           umma_f16_ta(t_o, t_s + (gp % NSP) * SUB + kk * 8, bd, ID_PV, !(first && kk == 0));
         }
         umma_commit(&pv_done[gp % NSP]);
-        if constexpr (!T::FP8 && !T::RING_BY_MMA) umma_commit(&empty_v[gp % T::NRING]);
+        if constexpr (!T::FP8 && !T::V_BY_PV) umma_commit(&empty_v[gp % T::NV]);
       };
       for (int it = it_begin; it < it_end; ++it) {
         const int4 item = p.items[it];
@@ -656,11 +673,11 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         for (int j = 0; j < nsub; ++j, ++g) {
           uint32_t kbase;
           if constexpr (T::FP8) {
-            wait_bar(&ck_full[g % NSP], (g / NSP) & 1);
-            kbase = smem_addr(smem + T::OFF_CV + (g % NSP) * T::CV_BUF);
+            wait_bar(&ck_full[g % T::NCK], (g / T::NCK) & 1);
+            kbase = smem_addr(smem + T::OFF_CV + (g % T::NCK) * T::CV_BUF);
           } else {
-            const int slot = (int)(g % T::NRING);
-            wait_bar(&full_k[slot], (g / T::NRING) & 1);
+            const int slot = (int)(g % T::NK);
+            wait_bar(&full_k[slot], (g / T::NK) & 1);
             kbase = smem_addr(smem + T::OFF_K + slot * T::SLOT);
           }
           if (g >= (uint32_t)NSP) {  // the buffer holds P(g - NSP) until its PV has read it
@@ -676,7 +693,8 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
           }
           // the logits are ready; the K slot (or widened K buffer) of the step is free
           umma_commit(&s_full[g % NSP]);
-          if constexpr (!T::FP8 && !T::RING_BY_MMA) umma_commit(&empty_k[g % T::NRING]);
+          if constexpr (T::FP8 && !T::CK_BY_S) umma_commit(&ck_free[g % T::NCK]);
+          if constexpr (!T::FP8 && !T::K_BY_S) umma_commit(&empty_k[g % T::NK]);
           if (j >= LAG) issue_pv(g - LAG, j == LAG);
         }
         for (int j = nsub > LAG ? nsub - LAG : 0; j < nsub; ++j) issue_pv(g_item + j, j == 0);
@@ -771,7 +789,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         if (!T::FP8 && nv < SUB) {
           // the zeroing below writes into the V slot: the tile must have landed (this wait
           // orders the writes after the copy)
-          wait_bar(&full_v[g % T::NRING], (g / T::NRING) & 1);
+          wait_bar(&full_v[g % T::NV], (g / T::NV) & 1);
         }
         wait_bar(&s_full[g % NSP], (g / NSP) & 1);
         tc_fence_after();
@@ -884,7 +902,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         if (!T::FP8 && nv < SUB) {
           // value rows past the item's tokens may hold anything: zero them (before this
           // step's PV reads them) so that zero weights stay zero
-          char* vt = smem + T::OFF_V + (g % T::NRING) * T::SLOT;
+          char* vt = smem + T::OFF_V + (g % T::NV) * T::SLOT;
           for (int e = stid; e < (SUB - nv) * T::NSLAB * 8; e += 128) {
             const int rr = nv + e / (T::NSLAB * 8), sl = (e / 8) % T::NSLAB, c = e & 7;
             *reinterpret_cast<uint4*>(vt + sl * T::KSLAB + sw128_chunk(rr, c)) =
@@ -1034,11 +1052,11 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       pend[2] = pend_odd.x;
       pend[3] = pend_odd.y;
     }
-  } else {
+  } else if (warp < T::W_CONV + T::NCW) {
     // ================================================================ fp8 widening
     if constexpr (T::FP8) {
-      // step g: the e4m3 K rows of ring slot g % NRING become the f16 rows of K buffer
-      // g % NSP, then its V rows those of V buffer g % NSP (rows past the item's tokens
+      // step g: the e4m3 K rows of ring slot g % NK become the f16 rows of K buffer
+      // g % NCK, then its V rows those of V buffer g % NSP (rows past the item's tokens
       // become zero); the scales are applied to the logits and P, not here
       const int ctid = tid - T::W_CONV * 32;  // 0 .. 32 NCW - 1
       // one operand: 64 rows of 128 e4m3 codes -> two slabs of 64 rows of 64 f16 values
@@ -1071,30 +1089,32 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         const int nsub = ceil_div(t1 - t0, SUB);
         for (int j = 0; j < nsub; ++j, ++g) {
           const int nv = min(SUB, t1 - (t0 + j * SUB));
-          const int slot = (int)(g % T::NRING);
-          const uint32_t ph = (g / T::NRING) & 1;
-          // ---- K rows (buffer g % NSP is free once the S of step g - NSP has completed)
-          wait_bar(&full_k[slot], ph);
-          if (g >= (uint32_t)NSP) {
-            const uint32_t x = g - NSP;
-            wait_bar(&s_full[x % NSP], (x / NSP) & 1);
+          const int slot = (int)(g % T::NK), vslot = (int)(g % T::NV);
+          // ---- K rows (buffer g % NCK is free once the S of step g - NCK has completed)
+          wait_bar(&full_k[slot], (g / T::NK) & 1);
+          if (g >= (uint32_t)T::NCK) {
+            const uint32_t x = g - T::NCK;
+            if constexpr (T::CK_BY_S)
+              wait_bar(&s_full[x % NSP], (x / NSP) & 1);
+            else
+              wait_bar(&ck_free[x % T::NCK], (x / T::NCK) & 1);
           }
-          widen(smem + T::OFF_K + slot * T::SLOT, smem + T::OFF_CV + (g % NSP) * T::CV_BUF, nv);
+          widen(smem + T::OFF_K + slot * T::SLOT, smem + T::OFF_CV + (g % T::NCK) * T::CV_BUF, nv);
           if (lane == 0) {
-            mbar_arrive(&ck_full[g % NSP]);
+            mbar_arrive(&ck_full[g % T::NCK]);
             mbar_arrive(&empty_k[slot]);  // this warp is done with the K slot
           }
           // ---- V rows (buffer g % NSP is free once the PV of step g - NSP has completed)
-          wait_bar(&full_v[slot], ph);
+          wait_bar(&full_v[vslot], (g / T::NV) & 1);
           if (g >= (uint32_t)NSP) {
             const uint32_t x = g - NSP;
             wait_bar(&pv_done[x % NSP], (x / NSP) & 1);
           }
-          widen(smem + T::OFF_V + slot * T::SLOT,
-                smem + T::OFF_CV + (NSP + g % NSP) * T::CV_BUF, nv);
+          widen(smem + T::OFF_V + vslot * T::SLOT,
+                smem + T::OFF_CV + (T::NCK + g % NSP) * T::CV_BUF, nv);
           if (lane == 0) {
             mbar_arrive(&cv_full[g % NSP]);
-            mbar_arrive(&empty_v[slot]);
+            mbar_arrive(&empty_v[vslot]);
           }
         }
       }

@@ -18,8 +18,6 @@ namespace pa {
 cudaError_t launch_simt_d64(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                             int, int, bool, cudaStream_t);
 int simt_ctas_per_sm_d64(int, int, bool);
-int simt_ctas_per_sm_d128(int, int, bool);
-int simt_ctas_per_sm_d256(int, int, bool);
 
 cudaError_t launch_tc_d128(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                            int, int, bool, cudaStream_t);
@@ -38,12 +36,9 @@ cudaError_t launch_mma_d128(const KernelParams&, const CUtensorMap&, const CUten
 cudaError_t launch_mma_d256(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
                             int, int, bool, cudaStream_t);
 
+// The CUDA-core kernel serves 64-dim fp8 caches only (rows shorter than a 128-byte slab).
 int simt_ctas_per_sm(int head_dim, int mp, int kvk, bool toks) {
-  switch (head_dim) {
-    case 64: return simt_ctas_per_sm_d64(mp, kvk, toks);
-    case 128: return simt_ctas_per_sm_d128(mp, kvk, toks);
-    default: return simt_ctas_per_sm_d256(mp, kvk, toks);
-  }
+  return head_dim == 64 ? simt_ctas_per_sm_d64(mp, kvk, toks) : 1;
 }
 
 int mma_ctas_per_sm(int head_dim, int mp, int kvk, bool toks) {
@@ -53,10 +48,6 @@ int mma_ctas_per_sm(int head_dim, int mp, int kvk, bool toks) {
     default: return mma_ctas_per_sm_d256(mp, kvk, toks);
   }
 }
-cudaError_t launch_simt_d128(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
-                             int, int, bool, cudaStream_t);
-cudaError_t launch_simt_d256(const KernelParams&, const CUtensorMap&, const CUtensorMap&, int, int,
-                             int, int, bool, cudaStream_t);
 
 KernelParams make_kernel_params(const DecodeArgs& a) {
   KernelParams p{};
@@ -116,12 +107,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& kmap, const CU
       default: return cudaErrorNotSupported;
     }
   }
-  switch (a.p.head_dim) {
-    case 64: return launch_simt_d64(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
-    case 128: return launch_simt_d128(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
-    case 256: return launch_simt_d256(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
-    default: return cudaErrorNotSupported;
-  }
+  if (a.p.head_dim == 64)
+    return launch_simt_d64(prm, kmap, vmap, a.v.ctas, a.v.mp, a.kv_kind, a.q_kind, toks, s);
+  return cudaErrorNotSupported;
 }
 
 namespace {
