@@ -572,8 +572,7 @@ def run_ours(args, rank, world, local):
             "dtype": compute_dtype(wl), "data": "synthetic",
             "config": workload_config(wl, statistics.fmean(b.step_bytes), l2_size(), world),
             "launch": {"grid_mult": int(b.cfg.grid_mult) or 1,
-                       "split_merge": "auto (the decode merges units of two pieces, the "
-                                      "reduce kernel the rest)",
+                       "split_merge": "auto (the reduce kernel merges every split unit)",
                        "timing": "device time of K CUDA-graph replays of the step (plan, "
                                  "decode, reduce)"},
             "roofline": roof,

@@ -89,8 +89,9 @@ typedef enum {
  * per unit; no CTA ever waits for another), or by pa_reduce's own kernel, which spreads the
  * rows of the unit over many CTAs.  The first costs no launch but runs on one SM, so it
  * suits units of a few pieces; the second suits units cut into many.
- *   PA_MERGE_AUTO (0, the default): pa_decode merges the units cut into two pieces;
- *     pa_reduce merges the units cut into more.
+ *   PA_MERGE_AUTO (0, the default): the library's choice, currently that of
+ *     PA_MERGE_IN_REDUCE (measured fastest: a merge inside the decode runs after the merging
+ *     CTA's own work and lengthens the decode's tail).
  *   PA_MERGE_IN_DECODE: pa_decode merges every unit and pa_reduce launches nothing.
  *   PA_MERGE_IN_REDUCE: pa_decode only writes partials and pa_reduce merges them all.
  * The choice changes the order of no sum inside a merge: outputs agree to rounding. */

@@ -67,18 +67,18 @@ int mma_ctas_per_sm(int head_dim, int mp, int kvk, bool toks);
 // Largest row tile of the tensor-core decode kernel.
 constexpr int kMmaMaxRows = 64;
 
-// Pieces of a split unit the decode kernel merges itself under PA_MERGE_AUTO.  The merge
-// runs on one SM after the CTA's other work while most of the grid may already be idle; a
-// unit of two pieces costs one extra partial there, but beyond that the reduce kernel, which
-// spreads every unit's rows over the whole GPU, finishes sooner (measured on 128-dim caches:
-// five-piece units of 16-row tiles took 10 us longer per step merged in the decode).
-constexpr int kDecodeMergePieces = 2;
-
-// The most pieces of a split unit the decode kernel merges itself (1: none).
-inline int decode_merge_limit(int split_merge) {
+// The most pieces of a split unit the decode kernel merges itself (1: none).  Under
+// PA_MERGE_AUTO every split unit is left to the reduce kernel: a merge inside the decode runs
+// on one SM after that CTA's own work (on the tcgen05 kernel, on the softmax warps, holding
+// the tensor-memory accumulator), so it lengthens the decode's tail, while the reduce kernel
+// spreads the rows of all split units over the GPU, a warp per row for units of few pieces
+// (measured on GB300, step times with the merge in the reduce kernel against two-piece units
+// merged in the decode: batched GQA 63.8 against 70.9 us, 64-row fp8 134 against 158 us,
+// head-dim-256 Sq = 64 B = 8 203 against 231 us, the rest equal).
+inline int decode_merge_limit(int split_merge, int path) {
+  (void)path;
   if (split_merge == PA_MERGE_IN_DECODE) return 1 << 30;
-  if (split_merge == PA_MERGE_IN_REDUCE) return 1;
-  return kDecodeMergePieces;
+  return 1;
 }
 
 // Query rows per kv head above which a 128-dim head runs on the tcgen05 kernel.
@@ -116,7 +116,7 @@ inline Variant make_variant(const pa_config& c) {
   v.ctas_per_sm = v.path == 2   ? 1
                   : v.path == 1 ? mma_ctas_per_sm(c.head_dim, v.mp, kvk, toks)
                                 : simt_ctas_per_sm(c.head_dim, v.mp, kvk, toks);
-  v.ns_dec = decode_merge_limit(c.split_merge);
+  v.ns_dec = decode_merge_limit(c.split_merge, v.path);
   v.ctas = 0;
   return v;
 }
@@ -124,13 +124,15 @@ inline Variant make_variant(const pa_config& c) {
 // ---------------------------------------------------------------------------------
 // Workspace layout (byte offsets from ws, every section 256-byte aligned).
 //   header     int32[64]: [0] flags, [1] chunk, [2] active CTAs, [3] items,
-//                         [4] units left to the reduce kernel
+//                         [4] units left to the reduce kernel, [5] how many of them have
+//                         at most kReduceWarpPieces pieces
 //   item_off   int32[C + 1]      first work item of each CTA
 //   items      int4[C + units]   (unit, t0, t1, partial slot or -1)
 //   unit_info  int2[units]       (slot of the first piece, number of pieces); piece s > 0
 //                                of a unit sits in slot 2 * (first / 2 + s)
 //   unit_cnt   int32[units]      pieces of each unit finished so far (merge in decode)
-//   red_units  int32[units]      units the reduce kernel merges, in unit order
+//   red_units  int32[units]      units the reduce kernel merges: those of at most
+//                                kReduceWarpPieces pieces, then the others, each in unit order
 //   seq_start  int32[B + 1]      planner scratch for very large batches
 //   seq_len    int32[B]
 //   o_part     f32[2C * mp * D]  normalised partial outputs (CTA c: slots 2c, 2c + 1)
@@ -164,7 +166,13 @@ inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
   return L;
 }
 
-enum HeaderSlot { HDR_FLAGS = 0, HDR_CHUNK = 1, HDR_ACTIVE = 2, HDR_ITEMS = 3, HDR_NRED = 4 };
+enum HeaderSlot {
+  HDR_FLAGS = 0, HDR_CHUNK = 1, HDR_ACTIVE = 2, HDR_ITEMS = 3, HDR_NRED = 4, HDR_NRED_SMALL = 5
+};
+
+// Split units of at most this many pieces are merged by the reduce kernel one warp per row
+// (all of a row's pieces loaded at once); larger ones with eight warps per row.
+constexpr int kReduceWarpPieces = 16;
 
 // Division by a run-time constant d in [1, 2^31) of a dividend n in [0, 2^31) with one
 // multiply-high, add and shift (the round-up multiplier method of Granlund and Montgomery,

@@ -148,29 +148,37 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   cdiv.s = s_chunk_div[2];
 
   // 4. per unit: its pieces and the slot of its first partial, and the list of split units
-  //    too large for the decode's own merge
-  int nred = 0;
-  for (int base = 0; base < p.units; base += kPlanThreads) {
-    const int u = base + tid;
-    int ns = 0, first = 0;
-    if (u < p.units && flags == 0) {
-      const int b = p.ups_div.div(u), k = u - b * ups;
-      const int plen = pad(seq_len[b]);
-      const int st = seq_start[b] + k * stride(seq_len[b]);
-      if (plen > 0) {
-        const int c0 = cdiv.div(st);
-        ns = cdiv.div(st + plen - 1) - c0 + 1;
-        first = 2 * c0 + (c0 * chunk < st ? 1 : 0);  // the last item of CTA c0, or its first
+  //    too large for the decode's own merge: units of at most kReduceWarpPieces pieces
+  //    first (the reduce kernel merges their rows a warp each), then the others, each part
+  //    in unit order
+  int nred = 0, nsmall = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int base = 0; base < p.units; base += kPlanThreads) {
+      const int u = base + tid;
+      int ns = 0, first = 0;
+      if (u < p.units && flags == 0) {
+        const int b = p.ups_div.div(u), k = u - b * ups;
+        const int plen = pad(seq_len[b]);
+        const int st = seq_start[b] + k * stride(seq_len[b]);
+        if (plen > 0) {
+          const int c0 = cdiv.div(st);
+          ns = cdiv.div(st + plen - 1) - c0 + 1;
+          first = 2 * c0 + (c0 * chunk < st ? 1 : 0);  // the last item of CTA c0, or its first
+        }
       }
+      const bool small = ns <= kReduceWarpPieces;
+      const int to_reduce = (ns > p.ns_dec && small == (pass == 0)) ? 1 : 0;
+      const int excl = block_exclusive_scan(to_reduce, &tot, sh);
+      if (u < p.units) {
+        if (pass == 0) {
+          p.unit_info[u] = make_int2(first, ns);
+          p.unit_cnt[u] = 0;
+        }
+        if (to_reduce) p.red_units[nred + excl] = u;
+      }
+      nred += tot;
     }
-    const int to_reduce = ns > p.ns_dec ? 1 : 0;
-    const int excl = block_exclusive_scan(to_reduce, &tot, sh);
-    if (u < p.units) {
-      p.unit_info[u] = make_int2(first, ns);
-      p.unit_cnt[u] = 0;
-      if (to_reduce) p.red_units[nred + excl] = u;
-    }
-    nred += tot;
+    if (pass == 0) nsmall = nred;
   }
 
   // 5. work items, CTA by CTA
@@ -216,6 +224,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     p.hdr[HDR_ACTIVE] = active;
     p.hdr[HDR_ITEMS] = carry;
     p.hdr[HDR_NRED] = nred;
+    p.hdr[HDR_NRED_SMALL] = nsmall;
   }
 }
 

@@ -127,11 +127,77 @@ struct ReduceParams {
 
 constexpr int kReduceWarps = 8;
 
-// One CTA per (listed unit, row): warp w folds pieces w, w + 8, ... into a running
-// (max, weight sum, weighted sum) with lanes over the head dimension, four floats a lane,
-// loading the partials of four pieces at a time; the eight warps' results are then combined
-// in shared memory.  Rows of all listed units are spread over the grid, so a unit cut into
-// many pieces is merged by many SMs at once.  Every sum runs in a fixed order.
+// The listed units come in two parts (the planner's order): units of at most
+// kReduceWarpPieces pieces, then the rest.
+//  * Few pieces: one warp per (unit, row), lanes over the head dimension (four floats a
+//    lane); lane s holds piece s's log2-sum-exp, so the row's max and weights are one
+//    shuffle reduction, and every piece's partial row is loaded before any is used, so a
+//    row costs about one memory round trip.  Eight rows per CTA at a time.
+//  * Many pieces: one CTA per (unit, row): warp w folds pieces w, w + 8, ... into a running
+//    (max, weight sum, weighted sum), loading the partials of four pieces at a time; the
+//    eight warps' results are then combined in shared memory, so a unit cut into many pieces
+//    is merged by many SMs at once.
+// Every sum runs in a fixed order.
+template <int D, int QK>
+__device__ __forceinline__ void reduce_row_warp(const ReduceParams& p, int u, int r, int lane) {
+  constexpr int D4 = D / 4;
+  constexpr int NV = (D4 + 31) / 32;  // float4 columns per lane
+  const int rb = u % p.RB, rg = rb * p.MP + r;
+  if (rg >= p.M) return;  // uniform over the warp
+  const int2 info = p.unit_info[u];
+  const int ns = info.y;  // <= kReduceWarpPieces
+  const float ls = lane < ns ? p.lse_part[(size_t)piece_slot(info.x, lane) * p.MP + r] : -INFINITY;
+  float m = ls;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  const float wl = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+  float W = wl;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
+  // pieces in chunks of eight, every load of a chunk in flight before any is used
+  constexpr int CH = 8;
+  float4 acc[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < ns; s0 += CH) {
+    float4 o4[CH][NV];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int s = s0 + j;
+      const size_t part = s < ns ? (size_t)piece_slot(info.x, s) * p.MP + r : 0;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = lane + 32 * v;
+        o4[j][v] = (s < ns && c < D4) ? reinterpret_cast<const float4*>(p.o_part + part * D)[c]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const float x = __shfl_sync(kFull, wl, (s0 + j) & 31);  // 0 for pieces past ns
+      const float xw = s0 + j < ns ? x : 0.f;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        acc[v].x += xw * o4[j][v].x;
+        acc[v].y += xw * o4[j][v].y;
+        acc[v].z += xw * o4[j][v].z;
+        acc[v].w += xw * o4[j][v].w;
+      }
+    }
+  }
+  const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv;
+  const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int c = lane + 32 * v;
+    if (c < D4)
+      store_out4<QK>(p.out, row * D + 4 * c,
+                     make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv));
+  }
+  if (lane == 0 && p.lse) p.lse[row] = W > 0.f ? (m + fast_log2(W)) * kLn2 : -INFINITY;
+}
+
 template <int D, int QK>
 __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceParams p) {
   constexpr int D4 = D / 4;
@@ -142,10 +208,14 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
   // the next kernel may start launching now: it is held in its own grid_dependency_wait
   // until this grid has completed, and it cannot take the place of a CTA of this grid
   grid_dependents_launch();
-  const int nred = p.hdr[HDR_NRED];
+  const int nred = p.hdr[HDR_NRED], nsmall = p.hdr[HDR_NRED_SMALL];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int w = blockIdx.x; w < nred * p.MP; w += gridDim.x) {
-    const int u = p.red_units[w / p.MP], r = w % p.MP;
+  // few-piece units: a warp per row
+  for (int w = blockIdx.x * kReduceWarps + warp; w < nsmall * p.MP; w += gridDim.x * kReduceWarps)
+    reduce_row_warp<D, QK>(p, p.red_units[w / p.MP], w % p.MP, lane);
+  // many-piece units: a CTA per row
+  for (int w = blockIdx.x; w < (nred - nsmall) * p.MP; w += gridDim.x) {
+    const int u = p.red_units[nsmall + w / p.MP], r = w % p.MP;
     const int rb = u % p.RB, rg = rb * p.MP + r;
     if (rg >= p.M) continue;  // uniform over the CTA
     const int2 info = p.unit_info[u];

@@ -69,16 +69,15 @@ TILE_BYTES = 16384
 TC_STEP_TOKENS = 64
 ITEM_COST_TILES = 3
 TC_MIN_ROWS = 33
-DECODE_MERGE_PIECES = 2
+REDUCE_WARP_PIECES = 16
 
 
-def decode_merge_limit(split_merge: int) -> int:
-    """Most pieces of a split unit that the decode kernel merges itself (pa_split_merge)."""
+def decode_merge_limit(split_merge: int, tc: bool) -> int:
+    """Most pieces of a split unit that the decode kernel merges itself (pa_split_merge);
+    PA_MERGE_AUTO leaves every split unit to the reduce kernel, like PA_MERGE_IN_REDUCE."""
     if split_merge == pa.MERGE_IN_DECODE:
         return 1 << 30
-    if split_merge == pa.MERGE_IN_REDUCE:
-        return 1
-    return DECODE_MERGE_PIECES
+    return 1
 
 
 def variant(cfg: pa.PaConfig, ctas: int):
@@ -95,7 +94,7 @@ def variant(cfg: pa.PaConfig, ctas: int):
     tt = TC_STEP_TOKENS if tc else TILE_BYTES // (cfg.head_dim * bpe)
     cost = ITEM_COST_TILES * (TILE_BYTES // (cfg.head_dim * bpe))
     return dict(rows=rows, mp=mp, rb=rb, tt=tt, units=cfg.batch * cfg.num_kv_heads * rb,
-                ctas=ctas, ns_dec=decode_merge_limit(cfg.split_merge),
+                ctas=ctas, ns_dec=decode_merge_limit(cfg.split_merge, tc),
                 item_cost=-(-cost // tt) * tt)
 
 
@@ -140,6 +139,7 @@ def plan_view(ws: torch.Tensor, cfg: pa.PaConfig, ctas: int):
     unit_info = arr("unit_info", np.int32, 2 * U).reshape(-1, 2)
     unit_cnt = arr("unit_cnt", np.int32, U)
     n_red = int(hdr[4])
+    n_red_small = int(hdr[5])
     red_units = arr("red_units", np.int32, U)[:n_red]
     o_part = arr("o_part", np.float32, 2 * C * v["mp"] * cfg.head_dim).reshape(
         2 * C, v["mp"], cfg.head_dim)
@@ -147,6 +147,7 @@ def plan_view(ws: torch.Tensor, cfg: pa.PaConfig, ctas: int):
     return dict(v=v, flags=int(hdr[0]), chunk=int(hdr[1]), active=int(hdr[2]),
                 n_items=int(hdr[3]), item_off=item_off.copy(), items=items.copy(),
                 unit_info=unit_info.copy(), unit_cnt=unit_cnt.copy(), red_units=red_units.copy(),
+                n_red_small=n_red_small,
                 o_part=o_part.copy(), lse_part=lse_part.copy())
 
 

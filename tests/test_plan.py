@@ -19,7 +19,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_run import plan_view, run
+from gpu_run import REDUCE_WARP_PIECES, plan_view, run
 from pagedkv import random_problem
 
 pytestmark = pytest.mark.gpu
@@ -82,8 +82,12 @@ def check_plan(view, ctx, ctas, hkv):
         elif ns > 1:
             first = int(info[0])
             assert slots[u] == [first] + [2 * (first // 2 + s) for s in range(1, ns)]
-    want_red = [u for u in range(U) if int(view["unit_info"][u][1]) > v["ns_dec"]]
-    assert view["red_units"].tolist() == want_red
+    # units left to the reduce kernel: the few-piece ones first, then the rest, each in order
+    ns_of = [int(view["unit_info"][u][1]) for u in range(U)]
+    small = [u for u in range(U) if v["ns_dec"] < ns_of[u] <= REDUCE_WARP_PIECES]
+    large = [u for u in range(U) if ns_of[u] > max(v["ns_dec"], REDUCE_WARP_PIECES)]
+    assert view["red_units"].tolist() == small + large
+    assert view["n_red_small"] == len(small)
     assert (view["unit_cnt"] == 0).all(), "merge counters not reset by the decode"
     return T
 
