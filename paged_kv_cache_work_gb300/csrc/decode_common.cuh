@@ -240,7 +240,18 @@ struct TileProducer {
       cp_async_arrive_noinc(&qfull[qs]);
     }
     char* st = smem + s * T::STAGE;
-    if (lane == 0) mbar_arrive_expect_tx(&full[s], nvalid * 2u * box_bytes);
+    // per-token scales of one kv head on a page that holds the whole tile: two contiguous
+    // runs of TT floats, copied by two bulk copies that complete on the stage's barrier
+    bool scale_bulk = false, ok0 = false;
+    if constexpr (TOKS) {
+      scale_bulk = p->Hkv == 1 && box_rows == T::TT &&
+                   ((reinterpret_cast<uintptr_t>(p->k_scale) |
+                     reinterpret_cast<uintptr_t>(p->v_scale)) & 15) == 0;
+      ok0 = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;  // lane 0's box is the tile's one page
+    }
+    if (lane == 0)
+      mbar_arrive_expect_tx(&full[s], nvalid * 2u * box_bytes +
+                                          (scale_bulk && ok0 ? 2u * T::TT * 4u : 0u));
     __syncwarp();
     if (ok) {
       // slab h of page j lands at h * (TT rows) + j * (box rows), in units of ROWB bytes
@@ -253,6 +264,17 @@ struct TileProducer {
     if constexpr (TOKS) {
       float* sks = reinterpret_cast<float*>(st + 2 * T::KTILE);
       float* svs = sks + T::TT;
+      if (scale_bulk) {
+        if (lane == 0 && ok0) {
+          const size_t idx = (size_t)blk * p->bs + (tokb & (p->bs - 1));
+          bulk_load_1d(sks, p->k_scale + idx, T::TT * 4, &full[s]);
+          bulk_load_1d(svs, p->v_scale + idx, T::TT * 4, &full[s]);
+        }
+        mbar_arrive(&full[s]);  // the 32 arrivals the stage expects besides the copy's
+        ++issued;
+        if (++k >= ntiles) have = false;
+        return true;
+      }
       for (int t = lane; t < T::TT; t += 32) {
         const int bb = __shfl_sync(kFull, blk, (t / box_rows) * T::NSLAB);
         const int tok = tok0 + t;
