@@ -8,6 +8,8 @@
 // Units the decode finished in one piece are skipped; units with no keys at all (a
 // sequence with no context) get zero rows and lse = -inf.  Sums over splits run in a fixed
 // order (lane-strided, then a fixed shuffle tree), so repeated calls are bitwise identical.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -139,28 +141,16 @@ constexpr int kReduceWarps = 8;
 //    is merged by many SMs at once.
 // Every sum runs in a fixed order.
 template <int D, int QK>
-__device__ __forceinline__ void reduce_row_warp(const ReduceParams& p, int u, int r, int lane) {
+__device__ __forceinline__ void reduce_row_warp(const ReduceParams& p, int u, int2 info, int r,
+                                                int lane) {
   constexpr int D4 = D / 4;
   constexpr int NV = (D4 + 31) / 32;  // float4 columns per lane
+  constexpr int CH = 8;               // pieces loaded at once
   const int rb = u % p.RB, rg = rb * p.MP + r;
   if (rg >= p.M) return;  // uniform over the warp
-  const int2 info = p.unit_info[u];
   const int ns = info.y;  // <= kReduceWarpPieces
-  const float ls = lane < ns ? p.lse_part[(size_t)piece_slot(info.x, lane) * p.MP + r] : -INFINITY;
-  float m = ls;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-  const float wl = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
-  float W = wl;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
-  // pieces in chunks of eight, every load of a chunk in flight before any is used
-  constexpr int CH = 8;
-  float4 acc[NV];
-#pragma unroll
-  for (int v = 0; v < NV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += CH) {
-    float4 o4[CH][NV];
+  float4 o4[CH][NV];
+  auto load_chunk = [&](int s0) {
 #pragma unroll
     for (int j = 0; j < CH; ++j) {
       const int s = s0 + j;
@@ -172,6 +162,22 @@ __device__ __forceinline__ void reduce_row_warp(const ReduceParams& p, int u, in
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
+  };
+  // the row's log2-sum-exps and its first pieces' partial rows are all in flight together
+  const float ls = lane < ns ? p.lse_part[(size_t)piece_slot(info.x, lane) * p.MP + r] : -INFINITY;
+  load_chunk(0);
+  float m = ls;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  const float wl = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+  float W = wl;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
+  float4 acc[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < ns; s0 += CH) {
+    if (s0 > 0) load_chunk(s0);
 #pragma unroll
     for (int j = 0; j < CH; ++j) {
       const float x = __shfl_sync(kFull, wl, (s0 + j) & 31);  // 0 for pieces past ns
@@ -204,21 +210,40 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
   constexpr int NV = (D4 + 31) / 32;  // float4 columns per lane
   __shared__ float s_m[kReduceWarps], s_w[kReduceWarps];
   __shared__ float4 s_acc[kReduceWarps][D4];
+  // The work list (header, reduce list, unit table) is the planner's, and the planner has
+  // finished before this grid starts: this grid starts once every CTA of the decode grid
+  // has passed its own wait on the planner.  So the list is read before this grid's wait,
+  // through L2 (these lines may sit stale in an SM's L1 from an earlier step), and only the
+  // partials, which the decode writes, after it.
+  const int nred = __ldcg(&p.hdr[HDR_NRED]), nsmall = __ldcg(&p.hdr[HDR_NRED_SMALL]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ws0 = blockIdx.x * kReduceWarps + warp, wl0 = blockIdx.x;
+  int us0 = 0, ul0 = 0;
+  int2 infos0 = make_int2(0, 0), infol0 = make_int2(0, 0);
+  if (ws0 < nsmall * p.MP) {
+    us0 = __ldcg(&p.red_units[ws0 / p.MP]);
+    infos0 = __ldcg(&p.unit_info[us0]);
+  }
+  if (wl0 < (nred - nsmall) * p.MP) {
+    ul0 = __ldcg(&p.red_units[nsmall + wl0 / p.MP]);
+    infol0 = __ldcg(&p.unit_info[ul0]);
+  }
   grid_dependency_wait();  // partials come from the decode kernel launched just before
   // the next kernel may start launching now: it is held in its own grid_dependency_wait
   // until this grid has completed, and it cannot take the place of a CTA of this grid
   grid_dependents_launch();
-  const int nred = p.hdr[HDR_NRED], nsmall = p.hdr[HDR_NRED_SMALL];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // few-piece units: a warp per row
-  for (int w = blockIdx.x * kReduceWarps + warp; w < nsmall * p.MP; w += gridDim.x * kReduceWarps)
-    reduce_row_warp<D, QK>(p, p.red_units[w / p.MP], w % p.MP, lane);
+  for (int w = ws0; w < nsmall * p.MP; w += gridDim.x * kReduceWarps) {
+    const int u = w == ws0 ? us0 : __ldcg(&p.red_units[w / p.MP]);
+    const int2 info = w == ws0 ? infos0 : __ldcg(&p.unit_info[u]);
+    reduce_row_warp<D, QK>(p, u, info, w % p.MP, lane);
+  }
   // many-piece units: a CTA per row
-  for (int w = blockIdx.x; w < (nred - nsmall) * p.MP; w += gridDim.x) {
-    const int u = p.red_units[nsmall + w / p.MP], r = w % p.MP;
+  for (int w = wl0; w < (nred - nsmall) * p.MP; w += gridDim.x) {
+    const int u = w == wl0 ? ul0 : __ldcg(&p.red_units[nsmall + w / p.MP]), r = w % p.MP;
     const int rb = u % p.RB, rg = rb * p.MP + r;
     if (rg >= p.M) continue;  // uniform over the CTA
-    const int2 info = p.unit_info[u];
+    const int2 info = w == wl0 ? infol0 : __ldcg(&p.unit_info[u]);
     float m = -INFINITY, W = 0.f;
     float4 acc[NV];
 #pragma unroll
@@ -349,7 +374,10 @@ cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s) {
   p.RB = a.v.rb;
   p.MP = a.v.mp;
   if (a.v.units == 0) return cudaSuccess;
-  // (unit, row) pairs never exceed units x mp; eight CTAs per SM cover them in a few rounds
+  // Rows to merge: few-piece units take a warp per (unit, row), so at most units x mp / 8
+  // CTAs; many-piece units a CTA per row, and as a unit of more than kReduceWarpPieces
+  // pieces holds that many of the 2C partial slots, at most 2C / (kReduceWarpPieces + 1)
+  // units are of that kind.  Eight CTAs per SM at most; the CTAs loop past that.
   int sms = a.v.sms;
   if (sms <= 0) {
     int dev = 0;
@@ -357,8 +385,12 @@ cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return cudaErrorUnknown;
   }
-  const long long pairs = (long long)a.v.units * a.v.mp;
-  const int grid = (int)(pairs < 8LL * sms ? pairs : 8LL * sms);
+  const long long units = a.v.units, mp = a.v.mp;
+  const long long large_units =
+      std::min(units, 2LL * a.v.ctas / (kReduceWarpPieces + 1));
+  const long long need = std::max((units * mp + kReduceWarps - 1) / kReduceWarps,
+                                  large_units * mp);
+  const int grid = (int)std::max(1LL, std::min(need, 8LL * sms));
   switch (a.p.head_dim) {
     case 64: return launch_reduce_d<64>(p, a.q_kind, grid, s);
     case 128: return launch_reduce_d<128>(p, a.q_kind, grid, s);
