@@ -221,6 +221,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
+// tmem_ld32 in two halves, so that independent work can run while the load is in flight:
+// the issue, and the wait, which takes the destination registers as operands so that no use
+// of them can be moved above it.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -802,17 +827,43 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         if (!warp_dead) {
           const uint32_t t_sg = t_s + (g % NSP) * SUB + lane_off;
           float x[NL];
-          if constexpr (NL == 64)
+          // per-token scales of this stream's keys and values (two streams): read from shared
+          // memory while the logits are on their way from tensor memory
+          float ksc[NL], vsc[NL];
+          constexpr bool SC_REG = T::TOKS && NL == 32;
+          if constexpr (NL == 64) {
             tmem_ld64(t_sg, x);
-          else
+          } else if constexpr (SC_REG) {
+            uint32_t xr[32];
+            tmem_ld32_issue(t_sg + c0, xr);
+#pragma unroll
+            for (int i = 0; i < NL / 4; ++i) {
+              const float4 k4 = *reinterpret_cast<const float4*>(sks + c0 + 4 * i);
+              const float4 v4 = *reinterpret_cast<const float4*>(sks + T::TT + c0 + 4 * i);
+              ksc[4 * i] = k4.x;
+              ksc[4 * i + 1] = k4.y;
+              ksc[4 * i + 2] = k4.z;
+              ksc[4 * i + 3] = k4.w;
+              vsc[4 * i] = v4.x;
+              vsc[4 * i + 1] = v4.y;
+              vsc[4 * i + 2] = v4.z;
+              vsc[4 * i + 3] = v4.w;
+            }
+            tmem_ld32_wait(xr);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) x[jj] = __uint_as_float(xr[jj]);
+          } else {
             tmem_ld32(t_sg + c0, x);
+          }
           // ---- online softmax of this thread's logits (log2 units), two per instruction
           const float2 s2 = make_float2(qk_scale, qk_scale), z2 = make_float2(0.f, 0.f);
           if constexpr (T::TOKS) {
             // logit j of the step times its key's scale
 #pragma unroll
             for (int i = 0; i < NL / 4; ++i) {
-              const float4 k4 = *reinterpret_cast<const float4*>(sks + c0 + 4 * i);
+              const float4 k4 = SC_REG ? make_float4(ksc[4 * i], ksc[4 * i + 1], ksc[4 * i + 2],
+                                                     ksc[4 * i + 3])
+                                       : *reinterpret_cast<const float4*>(sks + c0 + 4 * i);
               const float2 a = ffma2(make_float2(x[4 * i], x[4 * i + 1]), s2, z2);
               const float2 c = ffma2(make_float2(x[4 * i + 2], x[4 * i + 3]), s2, z2);
               const float2 ya = ffma2(a, make_float2(k4.x, k4.y), z2);
@@ -867,7 +918,9 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
                 if constexpr (T::TOKS) {
                   // the value row's scale enters P (a stale scale past the item's tokens meets
                   // a zero weight and is dropped)
-                  const float2 v2 = *reinterpret_cast<const float2*>(svs + c0 + 32 * h + 2 * i);
+                  const float2 v2 =
+                      SC_REG ? make_float2(vsc[32 * h + 2 * i], vsc[32 * h + 2 * i + 1])
+                             : *reinterpret_cast<const float2*>(svs + c0 + 32 * h + 2 * i);
                   p0 = p0 == 0.f ? 0.f : p0 * v2.x;
                   p1 = p1 == 0.f ? 0.f : p1 * v2.y;
                 }
@@ -1059,20 +1112,32 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       // g % NCK, then its V rows those of V buffer g % NSP (rows past the item's tokens
       // become zero); the scales are applied to the logits and P, not here
       const int ctid = tid - T::W_CONV * 32;  // 0 .. 32 NCW - 1
-      // one operand: 64 rows of 128 e4m3 codes -> two slabs of 64 rows of 64 f16 values
+      // one operand: 64 rows of 128 e4m3 codes -> two slabs of 64 rows of 64 f16 values.
+      // Lane l of a warp takes 16-byte chunk l % 8 of a row, so each group of eight lanes
+      // reads one 128-byte row.  Every load is issued before the first conversion: the
+      // compiler does not move a shared-memory load above a store to shared memory by
+      // itself, and with one load, its conversions and its stores after another the
+      // widening set the step's pace (measured: per-tensor fp8 Sq = 4 decode 94.8 us ->
+      // 83.5 us; writing the second slab's two chunks in the opposite order, to spread the
+      // stores over the banks, measured slower).
       auto widen = [&](const char* src, char* dst, int nv) {
+        constexpr int NIT = SUB * 8 / (32 * T::NCW);
+        uint4 w[NIT];
 #pragma unroll
-        for (int k = 0; k < SUB * 8 / (32 * T::NCW); ++k) {
+        for (int k = 0; k < NIT; ++k) {
           const int e = ctid + k * 32 * T::NCW;
-          const int rr = e / 8, c = e & 7;
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-          if (rr < nv) {
-            const uint4 w = *reinterpret_cast<const uint4*>(src + sw128_chunk(rr, c));
-            lo = make_uint4(e4m3x2_to_h2(w.x), e4m3x2_to_h2(w.x >> 16), e4m3x2_to_h2(w.y),
-                            e4m3x2_to_h2(w.y >> 16));
-            hi = make_uint4(e4m3x2_to_h2(w.z), e4m3x2_to_h2(w.z >> 16), e4m3x2_to_h2(w.w),
-                            e4m3x2_to_h2(w.w >> 16));
-          }
+          const int rr = e >> 3, c = e & 7;
+          w[k] = rr < nv ? *reinterpret_cast<const uint4*>(src + sw128_chunk(rr, c))
+                         : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < NIT; ++k) {
+          const int e = ctid + k * 32 * T::NCW;
+          const int rr = e >> 3, c = e & 7;
+          const uint4 lo = make_uint4(e4m3x2_to_h2(w[k].x), e4m3x2_to_h2(w[k].x >> 16),
+                                      e4m3x2_to_h2(w[k].y), e4m3x2_to_h2(w[k].y >> 16));
+          const uint4 hi = make_uint4(e4m3x2_to_h2(w[k].z), e4m3x2_to_h2(w[k].z >> 16),
+                                      e4m3x2_to_h2(w[k].w), e4m3x2_to_h2(w[k].w >> 16));
           // dims 16c .. 16c + 15 -> f16 slab c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1
           char* d = dst + (c >> 2) * T::CV_SLAB;
           *reinterpret_cast<uint4*>(d + sw128_chunk(rr, 2 * (c & 3))) = lo;
