@@ -24,6 +24,7 @@ struct KernelParams {
   void* out;
   float* lse;
   const int32_t* item_off;
+  const int4* first_item;  // [C]: item item_off[c] of CTA c, or (0, 0, 0, -1)
   const int4* items;
   float* o_part;
   float* lse_part;
@@ -162,7 +163,7 @@ struct TileProducer {
   __device__ __forceinline__ void init(const KernelParams* prm, const CUtensorMap* km,
                                        const CUtensorMap* vm, char* sm, uint64_t* f,
                                        uint64_t* e, uint64_t* qf, volatile int* ab, int ln,
-                                       int ib, int ie) {
+                                       int ib, int ie, int4 first) {
     p = prm; kmap = km; vmap = vm; smem = sm; full = f; empty = e; qfull = qf; abort_flag = ab;
     lane = ln; it = ib - 1; it_end = ie; k = 0; ntiles = 0; issued = 0; items_started = 0;
     box_rows = min(p->bs, T::TT);
@@ -170,7 +171,7 @@ struct TileProducer {
     box_bytes = (uint32_t)box_rows * T::ROWB;
     have = false;
     next_ready = false;
-    item_next = ib < ie ? p->items[ib] : make_int4(0, 0, 0, -1);
+    item_next = first;  // item ib, or (0, 0, 0, -1)
   }
 
   // Move to the next item with tokens; false when the CTA's list is exhausted.

@@ -177,10 +177,13 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   // until this grid has completed, and it cannot take the place of a CTA of this grid
   grid_dependents_launch();
 
+  // the CTA's item range and its first item, read together (one round trip)
   const int it_begin = p.item_off[blockIdx.x], it_end = p.item_off[blockIdx.x + 1];
+  const int4 first = p.first_item[blockIdx.x];
   TileProducer<T> prod;
   if (warp == 0) {
-    prod.init(&p, &kmap, &vmap, smem, full, empty, qfull, abort_flag, lane, it_begin, it_end);
+    prod.init(&p, &kmap, &vmap, smem, full, empty, qfull, abort_flag, lane, it_begin, it_end,
+              first);
     prod.fill(T::NSTAGE - 1);
   }
   const bool tensor_scale = p.scale_mode == PA_SCALE_PER_TENSOR;
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(MmaTraits<D, MP, KVK, TOKS>::NTHREADS, 2)
   int2 pend_even = make_int2(-1, 0), pend_odd = make_int2(-1, 0);  // held by thread 32
 
   // the next item and its sequence's lengths are read one item ahead
-  int4 item_next = it_begin < it_end ? p.items[it_begin] : make_int4(0, 0, 0, -1);
+  int4 item_next = first;
   int n_next = 0, ql_next = 0;
   if (it_begin < it_end) {
     const int bn = item_next.x / (p.Hkv * p.RB);

@@ -362,7 +362,8 @@ struct TcProducer {
   __device__ __forceinline__ void init(const KernelParams* prm, const CUtensorMap* km,
                                        const CUtensorMap* vm, char* sm, uint64_t* fk,
                                        uint64_t* rk, uint64_t* fv, uint64_t* rv, uint64_t* scf,
-                                       uint64_t* scr, volatile int* ab, int ln, int ib, int ie) {
+                                       uint64_t* scr, volatile int* ab, int ln, int ib, int ie,
+                                       int4 first) {
     kmap = km; vmap = vm; smem = sm; full_k = fk; rel_k = rk; full_v = fv; rel_v = rv;
     sc_full = scf; sc_free = scr; abort_flag = ab; lane = ln;
     flags = prm->flags; bt = prm->bt; items = prm->items; kscale = prm->k_scale;
@@ -377,7 +378,7 @@ struct TcProducer {
     it = ib - 1;
     it_end = ie;
     have = false;
-    item_next = ib < ie ? items[ib] : make_int4(0, 0, 0, -1);
+    item_next = first;  // item ib, or (0, 0, 0, -1)
     last_b = -1;
     last_page = -1;
     last_blk = -1;
@@ -634,7 +635,9 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   // until this grid has completed, and it cannot take the place of a CTA of this grid
   grid_dependents_launch();
 
+  // the CTA's item range and its first item, read together (one round trip)
   const int it_begin = p.item_off[blockIdx.x], it_end = p.item_off[blockIdx.x + 1];
+  const int4 first = p.first_item[blockIdx.x];
   auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
     if (!mbar_wait(bar, parity, abort_flag)) {
       atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
@@ -647,7 +650,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     TcProducer<T> prod;
     prod.init(&p, &kmap, &vmap, smem, full_k, T::K_BY_S ? s_full : empty_k, full_v,
               T::V_BY_PV ? pv_done : empty_v, sc_full, sc_free, abort_flag, lane, it_begin,
-              it_end);
+              it_end, first);
     prod.run();  // every tile of the work list, as slots come free
     prod.drain();
   } else if (warp == T::W_MMA) {
@@ -684,7 +687,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         if constexpr (!T::FP8 && !T::V_BY_PV) umma_commit(&empty_v[gp % T::NV]);
       };
       for (int it = it_begin; it < it_end; ++it) {
-        const int4 item = p.items[it];
+        const int4 item = it == it_begin ? first : p.items[it];
         const int t0 = item.y, t1 = item.z;
         if (t1 <= t0) continue;
         const int nsub = ceil_div(t1 - t0, SUB);
@@ -753,7 +756,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       tc_fence_after();
     };
     int2 pend_even = make_int2(-1, 0), pend_odd = make_int2(-1, 0);  // held by stid 0
-    int4 item_next = it_begin < it_end ? p.items[it_begin] : make_int4(0, 0, 0, -1);
+    int4 item_next = first;
     for (int it = it_begin; it < it_end; ++it) {
       const int4 item = item_next;
       if (it + 1 < it_end) item_next = p.items[it + 1];
@@ -1148,7 +1151,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       };
       uint32_t g = 0;
       for (int it = it_begin; it < it_end; ++it) {
-        const int4 item = p.items[it];
+        const int4 item = it == it_begin ? first : p.items[it];
         const int t0 = item.y, t1 = item.z;
         if (t1 <= t0) continue;
         const int nsub = ceil_div(t1 - t0, SUB);

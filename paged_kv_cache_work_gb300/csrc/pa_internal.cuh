@@ -127,6 +127,8 @@ inline Variant make_variant(const pa_config& c) {
 //                         [4] units left to the reduce kernel, [5] how many of them have
 //                         at most kReduceWarpPieces pieces
 //   item_off   int32[C + 1]      first work item of each CTA
+//   first_item int4[C]           each CTA's first work item again ((0, 0, 0, -1) if none), so
+//                                that a CTA reads it together with its offsets
 //   items      int4[C + units]   (unit, t0, t1, partial slot or -1)
 //   unit_info  int2[units]       (slot of the first piece, number of pieces); piece s > 0
 //                                of a unit sits in slot 2 * (first / 2 + s)
@@ -138,8 +140,8 @@ inline Variant make_variant(const pa_config& c) {
 //   o_part     f32[2C * mp * D]  normalised partial outputs (CTA c: slots 2c, 2c + 1)
 //   lse_part   f32[2C * mp]      their log2-sum-exp
 struct WsLayout {
-  size_t header, item_off, items, unit_info, unit_cnt, red_units, seq_start, seq_len, o_part,
-      lse_part, total;
+  size_t header, item_off, first_item, items, unit_info, unit_cnt, red_units, seq_start, seq_len,
+      o_part, lse_part, total;
 };
 
 inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
@@ -153,6 +155,7 @@ inline WsLayout ws_layout(const pa_config& c, const Variant& v) {
   const size_t max_items = (size_t)v.ctas + (size_t)v.units;
   L.header = take(64 * sizeof(int32_t));
   L.item_off = take(((size_t)v.ctas + 1) * sizeof(int32_t));
+  L.first_item = take((size_t)v.ctas * sizeof(int4));
   L.items = take(max_items * sizeof(int4));
   L.unit_info = take((size_t)v.units * sizeof(int2));
   L.unit_cnt = take((size_t)v.units * sizeof(int32_t));

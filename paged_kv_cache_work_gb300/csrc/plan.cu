@@ -36,6 +36,7 @@ struct PlanParams {
   const int32_t* qlens;
   int32_t* hdr;
   int32_t* item_off;
+  int4* first_item;
   int4* items;
   int2* unit_info;
   int32_t* unit_cnt;
@@ -271,6 +272,7 @@ __global__ void __launch_bounds__(kPlanMaxThreads, 1) plan_kernel(const PlanPara
     int uf = uf0, lo = lo0, hi = hi0, n = n0;
     if (c != cb) n = cta_units(c, uf, lo, hi);
     p.item_off[c] = at;
+    if (n == 0) p.first_item[c] = make_int4(0, 0, 0, -1);
     for (int k = 0; k < n; ++k) {
       const int u = uf + k;
       const int b = p.ups_div.div(u), ku = u - b * ups;
@@ -288,7 +290,9 @@ __global__ void __launch_bounds__(kPlanMaxThreads, 1) plan_kernel(const PlanPara
           slot = 2 * c + (k > 0 ? 1 : 0);
         }
       }
-      p.items[at++] = make_int4(u, t0, t1, slot);
+      const int4 item = make_int4(u, t0, t1, slot);
+      if (k == 0) p.first_item[c] = item;
+      p.items[at++] = item;
     }
   }
   if (tid == 0) {
@@ -311,6 +315,7 @@ cudaError_t launch_plan(const ProblemArgs& a, const Variant& v, const WsLayout& 
   p.qlens = a.q_lens;
   p.hdr = reinterpret_cast<int32_t*>(ws + L.header);
   p.item_off = reinterpret_cast<int32_t*>(ws + L.item_off);
+  p.first_item = reinterpret_cast<int4*>(ws + L.first_item);
   p.items = reinterpret_cast<int4*>(ws + L.items);
   p.unit_info = reinterpret_cast<int2*>(ws + L.unit_info);
   p.unit_cnt = reinterpret_cast<int32_t*>(ws + L.unit_cnt);

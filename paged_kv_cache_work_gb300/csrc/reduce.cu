@@ -62,6 +62,7 @@ KernelParams make_kernel_params(const DecodeArgs& a) {
   p.out = a.out;
   p.lse = a.lse;
   p.item_off = reinterpret_cast<const int32_t*>(a.ws + a.L.item_off);
+  p.first_item = reinterpret_cast<const int4*>(a.ws + a.L.first_item);
   p.items = reinterpret_cast<const int4*>(a.ws + a.L.items);
   p.o_part = reinterpret_cast<float*>(a.ws + a.L.o_part);
   p.lse_part = reinterpret_cast<float*>(a.ws + a.L.lse_part);

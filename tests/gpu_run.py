@@ -110,6 +110,7 @@ def layout(cfg: pa.PaConfig, v: dict):
     C, U = v["ctas"], v["units"]
     take("header", 64 * 4)
     take("item_off", (C + 1) * 4)
+    take("first_item", C * 16)
     take("items", (C + U) * 16)
     take("unit_info", U * 8)
     take("unit_cnt", U * 4)
@@ -135,6 +136,7 @@ def plan_view(ws: torch.Tensor, cfg: pa.PaConfig, ctas: int):
     C, U = v["ctas"], v["units"]
     hdr = arr("header", np.int32, 64)
     item_off = arr("item_off", np.int32, C + 1)
+    first_item = arr("first_item", np.int32, 4 * C).reshape(-1, 4)
     items = arr("items", np.int32, 4 * (C + U)).reshape(-1, 4)
     unit_info = arr("unit_info", np.int32, 2 * U).reshape(-1, 2)
     unit_cnt = arr("unit_cnt", np.int32, U)
@@ -145,7 +147,8 @@ def plan_view(ws: torch.Tensor, cfg: pa.PaConfig, ctas: int):
         2 * C, v["mp"], cfg.head_dim)
     lse_part = arr("lse_part", np.float32, 2 * C * v["mp"]).reshape(2 * C, v["mp"])
     return dict(v=v, flags=int(hdr[0]), chunk=int(hdr[1]), active=int(hdr[2]),
-                n_items=int(hdr[3]), item_off=item_off.copy(), items=items.copy(),
+                n_items=int(hdr[3]), item_off=item_off.copy(), first_item=first_item.copy(),
+                items=items.copy(),
                 unit_info=unit_info.copy(), unit_cnt=unit_cnt.copy(), red_units=red_units.copy(),
                 n_red_small=n_red_small,
                 o_part=o_part.copy(), lse_part=lse_part.copy())

@@ -46,6 +46,10 @@ def check_plan(view, ctx, ctas, hkv):
     item_off, items = view["item_off"], view["items"]
     assert item_off[0] == 0 and (np.diff(item_off) >= 0).all()
     assert item_off[-1] == view["n_items"]
+    # each CTA's first item is repeated in its own slot, (0, 0, 0, -1) for an empty list
+    for c in range(ctas):
+        want_first = items[item_off[c]] if item_off[c] < item_off[c + 1] else [0, 0, 0, -1]
+        assert view["first_item"][c].tolist() == list(want_first), f"CTA {c} first item"
     covered = [np.zeros(int(n), np.int32) for n in lens]
     slots = {}
     for c in range(ctas):
