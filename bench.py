@@ -430,7 +430,10 @@ class Bench:
                 "decode_timing": ("back-to-back launches, CUDA events around the batch"
                                   if stream_ms is not None else "one launch per event pair"),
                 "decode_us_isolated_mean": round(statistics.fmean(decode_ms) * 1e3, 2),
-                "decode_us_isolated_median": round(statistics.median(decode_ms) * 1e3, 2)}
+                "decode_us_isolated_median": round(statistics.median(decode_ms) * 1e3, 2),
+                # each input set's algorithmic bytes (launches alternate the sets, set 0
+                # first: odd-numbered launches read set 0), to hold a profiled launch against
+                "kv_bytes_per_set": [int(x) for x in self.step_bytes]}
 
 
 def measure_config(wl, dev, seed, steps, warmup, peak, peak_kind):
@@ -444,6 +447,7 @@ def measure_config(wl, dev, seed, steps, warmup, peak, peak_kind):
     step_s = sec / n
     entry = {"kernel": roof["kernel"], "q_dtype": wl.q_dtype, "kv_dtype": wl.kv_dtype,
              "scale_mode": wl.scale_mode, "kv_bytes_per_step": int(statistics.fmean(b.step_bytes)),
+             "kv_bytes_per_set": [int(x) for x in b.step_bytes],
              "steps": n, "step_us": round(step_s * 1e6, 2),
              "step_tbs": round(nbytes / sec / 1e12, 4),
              "step_frac": round(nbytes / sec / 1e9 / peak, 4),
