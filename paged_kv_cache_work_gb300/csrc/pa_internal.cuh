@@ -54,6 +54,15 @@ constexpr int kTcStepTokens = 64;
 // unit's epilogue and for refilling its copy pipeline (about 5 us at the ~22 GB/s one CTA
 // streams, or three tiles of K and V), so the planner counts every unit that long.
 constexpr int kItemCostTiles = 3;
+// The same for the tcgen05 kernel, in 64-token steps.  Per-CTA exit times against the number
+// of items a CTA holds put an extra item at about 5 us on the long-context Sq = 4 decode
+// (head dim 128, bf16) and 9-10 us on the head-dim-256 Sq = 64 one, both about 430 tokens of
+// the CTA's own streaming (the query rows into tensor memory, the last PVs, the two token
+// streams' merge and the output or partial); seven steps balance the CTAs' exits there (the
+// long-context decode went from 37.5 to 35.0 us).  fp8 steps, slower per token, balanced at
+// six steps and measured slightly slower at seven.
+constexpr int kTcItemCostSteps = 7;
+constexpr int kTcItemCostStepsFp8 = 6;
 
 inline int pow2_at_least(int x) {
   int p = 1;
@@ -108,8 +117,11 @@ inline Variant make_variant(const pa_config& c) {
     v.mp = v.rows <= kSimtMaxRows ? pow2_at_least(v.rows) : kSimtMaxRows;
   v.rb = ceil_div(v.rows, v.mp);
   v.tt = v.path == 2 ? kTcStepTokens : kTileBytes / (c.head_dim * v.bpe);
-  // the item cost is measured in 16 KB tiles of streaming, rounded up to whole tiles
-  v.item_cost = round_up(kItemCostTiles * (kTileBytes / (c.head_dim * v.bpe)), v.tt);
+  // the item cost is measured in 16 KB tiles of streaming (tcgen05: in steps), rounded up
+  // to whole tiles
+  v.item_cost =
+      v.path == 2 ? (v.bpe == 1 ? kTcItemCostStepsFp8 : kTcItemCostSteps) * kTcStepTokens
+                  : round_up(kItemCostTiles * (kTileBytes / (c.head_dim * v.bpe)), v.tt);
   v.units = c.batch * c.num_kv_heads * v.rb;
   const int kvk = c.kv_dtype == PA_FP8_E4M3 ? 2 : (c.kv_dtype == PA_FP16 ? 1 : 0);
   const bool toks = c.kv_scale_mode == PA_SCALE_PER_TOKEN;
