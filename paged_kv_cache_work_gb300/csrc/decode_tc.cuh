@@ -9,14 +9,17 @@
 //               scales into a small shared-memory ring of their own;
 //   warp 1      one thread issues, per step g, S = Q K^T (M = 128, N = 64, K = head dim)
 //               into tensor-memory buffer g % NSP, and then O += P V for step g - LAG
-//               (M = 128, N = head dim, K = 64, V read as an MN-major operand);
+//               (M = 128, N = head dim, K = 64, V read as an MN-major operand); for an fp8
+//               cache S is of kind f8f6f4 on the K codes as they landed, against the query
+//               row held as two E4M3 terms (hi + lo, exact for a bf16 query but for elements
+//               below about a thousandth of the row's largest);
 //   warps 2-5   the softmax: tensor-memory lane L is owned by one thread, which loads its
 //               logits with tcgen05.ld, runs the online softmax in registers and writes its
 //               row of P as 16-bit pairs over the first half of the same logits buffer; at
 //               the end of an item it loads O and writes the output or the split partial
 //               (merge protocol of decode_common.cuh);
-//   warps 6-9   (fp8 caches) widen each step's e4m3 K and V rows to f16 operands in shared
-//               memory (one warp per SM sub-partition).
+//   warps 6-9   (fp8 caches) widen each step's e4m3 V rows to f16 operands in shared memory
+//               (one warp per SM sub-partition).
 //
 // Issue cost.  The tensor pipe takes about 48 SM clocks for an N = 64 logits MMA and 64 for
 // an N = 128 one when they are issued back to back, but each tcgen05.commit costs it about
@@ -66,31 +69,29 @@ struct TcTraits {
   // released by the commit of the S (K) or the PV (V) of step g that the softmax and the MMA
   // thread wait for anyway.  Head dim 256: three slots (two S/P buffers fit in tensor
   // memory, two slots would leave too little in flight), released by commits of their own.
-  // fp8: three slots of codes, released by the widening warps (deeper fp8 rings, five slots
-  // or two K / seven V, measured no faster: the widening and the MMA set the pace).
-  static constexpr int NK = FP8 ? 3 : (D == 256 ? 3 : NSP);  // K ring slots
-  static constexpr int NV = FP8 ? 3 : (D == 256 ? 3 : NSP);  // V ring slots
-  static constexpr bool K_BY_S = !FP8 && NK == NSP;   // a K slot is released by its S's commit
+  // fp8: the logits MMA reads the K codes in their ring slot (NSP slots, released by the S's
+  // commit); the V codes are widened out of a ring of their own, released by the widening
+  // warps.
+  static constexpr int NK = D == 256 && !FP8 ? 3 : NSP;    // K ring slots
+  static constexpr int NV = FP8 ? 5 : (D == 256 ? 3 : NSP);  // V ring slots
+  static constexpr bool K_BY_S = NK == NSP;            // a K slot is released by its S's commit
   static constexpr bool V_BY_PV = !FP8 && NV == NSP;  // a V slot is released by its PV's commit
   static constexpr int ROWB = 128;             // swizzled slabs of 128 bytes per row
   static constexpr int NSLAB = D * BPE / 128;  // slabs of a cache tile row
   static constexpr int OFF_K = 0;                      // K ring
   static constexpr int OFF_V = OFF_K + NK * SLOT;      // V ring
-  // fp8: the widened (f16) K rows of NCK steps and V rows of NCV steps, 128-byte-swizzled
-  // operands of two 64-dim slabs.  Both are indexed by the step modulo NSP, so the K buffer
-  // of step g is released by the S's commit to s_full and the V buffer by the PV's commit to
-  // pv_done (with fewer K buffers they would need a commit of their own, which measured
-  // slower: a commit costs the tensor pipe about 90 clocks).
-  static constexpr int NCK = FP8 ? NSP : 0;
+  // fp8: the widened (f16) V rows of NCV steps, 128-byte-swizzled operands of two 64-dim
+  // slabs, indexed by the step modulo NSP, so that the buffer of step g is released by the
+  // PV's commit to pv_done.  The K codes are not widened: the logits MMA is of kind f8f6f4,
+  // with the query rows split into two E4M3 terms.
   static constexpr int NCV = FP8 ? NSP : 0;
-  static constexpr bool CK_BY_S = NCK == NSP;
   static constexpr int CV_SLAB = SUB * 128;
   static constexpr int CV_BUF = 2 * CV_SLAB;
   static constexpr int OFF_CV = OFF_V + NV * SLOT;     // K buffers, then V buffers
   static constexpr int SCRATCH = OFF_CV;  // bytes free for the merges at the end (the rings)
   static constexpr int KSLAB = FP8 ? CV_SLAB : TT * 128;  // slab stride of the MMA operands
   // two-stream merge: the second stream's O rows (fp32, 16-byte chunks swizzled by row)
-  static constexpr int OFF_MRG = OFF_CV + (NCK + NCV) * CV_BUF;
+  static constexpr int OFF_MRG = OFF_CV + NCV * CV_BUF;
   static constexpr int MRG_BYTES = DUAL ? 64 * D * 4 : 0;
   // per-token scales: NSC slots of 64 K then 64 V fp32 scales
   static constexpr int NSC = TOKS ? 8 : 0;
@@ -100,9 +101,9 @@ struct TcTraits {
   static constexpr int ML_BYTES = round_up(2 * MP * 4 + (DUAL ? 2 * 64 * 4 : 0), 128);
   static constexpr int OFF_BAR = round_up(OFF_ML + ML_BYTES, 64);
   // full_k, empty_k (NK each), full_v, empty_v (NV each), s_full, p_full, pv_done (NSP each),
-  // o_free, q_full, mma_end, ck_full and ck_free (NCK each), cv_full (NCV), sc_full and
+  // o_free, q_full, mma_end, cv_full (NCV), sc_full and
   // sc_free (NSC each)
-  static constexpr int NBAR = 2 * NK + 2 * NV + 3 * NSP + 3 + 2 * NCK + NCV + 2 * NSC;
+  static constexpr int NBAR = 2 * NK + 2 * NV + 3 * NSP + 3 + NCV + 2 * NSC;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 16 + 1024;
   static constexpr int CTAS_PER_SM = 1;
   // Tensor memory (lane = query row, 32-bit columns): NSP S/P buffers of SUB fp32 columns
@@ -118,10 +119,8 @@ struct TcTraits {
   static_assert(!FP8 || D == 128, "fp8 caches at head dim 128");
   static_assert(!FP8 || (SUB * 8) % (32 * (NCW > 0 ? NCW : 1)) == 0, "widening: whole passes");
   // the V rows of step g wait for the PV of step g - NSP, issued after the S of step
-  // g - NSP + LAG, which waits for the K rows of that step: the widening, K(g) then V(g),
-  // must not need K rows past g
+  // g - NSP + LAG: the PVs trail the S MMAs by fewer steps than there are buffers
   static_assert(LAG >= 1 && LAG < NSP, "no cycle between the roles");
-  static_assert(!FP8 || NCK >= 2, "the widening of K(g) waits only for the S of step g - NCK");
   static_assert(!FP8 || NCV == NSP, "a widened V buffer is released through pv_done");
   static_assert(MP == 64 || MP == 128, "row tile");
   static_assert(D == 128 || D == 256, "head dim");
@@ -156,6 +155,16 @@ __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0)
+      : "memory");
+}
+// kind::f8f6f4 with A in tensor memory (lane = row, a 32-bit column = four E4M3 K elements)
+// and B an E4M3 shared operand; the instruction descriptor's operand formats are 0 (E4M3).
+__device__ __forceinline__ void umma_f8_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0)
       : "memory");
 }
@@ -281,6 +290,14 @@ __device__ __forceinline__ uint32_t pack16x2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+}
+// Two fp32 values to two E4M3 codes (a -> low byte): round to nearest even, saturating.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n mov.b16 %0, t;\n}"
+      : "=h"(r)
+      : "f"(b), "f"(a));
+  return r;
 }
 // Two E4M3 codes (low byte first) to an f16 pair (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t w) {
@@ -555,6 +572,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   constexpr int NSP = T::NSP;
   constexpr bool BF = KVK == KV_BF16;  // MMA operands bf16 (else f16: f16 and fp8 caches)
   constexpr uint32_t ID_S = umma_idesc(128, SUB, BF, false);
+  constexpr uint32_t ID_S8 = umma_idesc(128, SUB, false, false);  // f8f6f4: E4M3 x E4M3
   constexpr uint32_t ID_PV = umma_idesc(128, D, BF, true);
   constexpr int SOFT_BAR = 2;  // named barrier of the four softmax warps
   extern __shared__ char smem_raw[];
@@ -569,9 +587,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   uint64_t* o_free = pv_done + NSP;
   uint64_t* q_full = o_free + 1;
   uint64_t* mma_end = q_full + 1;
-  uint64_t* ck_full = mma_end + 1;       // [NCK]: widened K rows of the step in buffer b
-  uint64_t* ck_free = ck_full + T::NCK;  // [NCK]: the S that read buffer b has completed
-  uint64_t* cv_full = ck_free + T::NCK;  // [NCV]: widened V rows of the step in buffer b
+  uint64_t* cv_full = mma_end + 1;       // [NCV]: widened V rows of the step in buffer b
   uint64_t* sc_full = cv_full + T::NCV;  // [NSC]: per-token scales of the step in slot b
   uint64_t* sc_free = sc_full + T::NSC;  // [NSC]: the softmax is done with slot b
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sc_free + T::NSC);
@@ -582,20 +598,16 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    // readers of a ring slot: the widening warps (fp8), or the commit of the S (K) or PV
+    // readers of a ring slot: the widening warps (fp8 V), or the commit of the S (K) or PV
     // (V) that read it when the ring is not released through s_full / pv_done; full: the
     // expect_tx arrival of the copy
     for (int s = 0; s < T::NK; ++s) {
       mbar_init(&full_k[s], 1);
-      mbar_init(&empty_k[s], T::FP8 ? T::NCW : 1);
+      mbar_init(&empty_k[s], 1);
     }
     for (int s = 0; s < T::NV; ++s) {
       mbar_init(&full_v[s], 1);
       mbar_init(&empty_v[s], T::FP8 ? T::NCW : 1);
-    }
-    for (int b = 0; b < T::NCK; ++b) {
-      mbar_init(&ck_full[b], T::NCW);
-      mbar_init(&ck_free[b], 1);
     }
     for (int b = 0; b < T::NCV; ++b) mbar_init(&cv_full[b], T::NCW);
     for (int b = 0; b < NSP; ++b) {
@@ -666,7 +678,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         uint32_t vaddr;
         if constexpr (T::FP8) {
           wait_bar(&cv_full[gp % NSP], (gp / NSP) & 1);
-          vaddr = smem_addr(smem + T::OFF_CV + (T::NCK + gp % NSP) * T::CV_BUF);
+          vaddr = smem_addr(smem + T::OFF_CV + (gp % NSP) * T::CV_BUF);
         } else {
           const int slot = (int)(gp % T::NV);
           wait_bar(&full_v[slot], (gp / T::NV) & 1);
@@ -699,30 +711,36 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         constexpr int LAG = T::LAG;
         const uint32_t g_item = g;  // the item's first step
         for (int j = 0; j < nsub; ++j, ++g) {
-          uint32_t kbase;
-          if constexpr (T::FP8) {
-            wait_bar(&ck_full[g % T::NCK], (g / T::NCK) & 1);
-            kbase = smem_addr(smem + T::OFF_CV + (g % T::NCK) * T::CV_BUF);
-          } else {
-            const int slot = (int)(g % T::NK);
-            wait_bar(&full_k[slot], (g / T::NK) & 1);
-            kbase = smem_addr(smem + T::OFF_K + slot * T::SLOT);
-          }
+          const int slot = (int)(g % T::NK);
+          wait_bar(&full_k[slot], (g / T::NK) & 1);
+          const uint32_t kbase = smem_addr(smem + T::OFF_K + slot * T::SLOT);
           if (g >= (uint32_t)NSP) {  // the buffer holds P(g - NSP) until its PV has read it
             const uint32_t x = g - NSP;
             wait_bar(&pv_done[x % NSP], (x / NSP) & 1);
           }
           tc_fence_after();
           const uint32_t t_sg = t_s + (g % NSP) * SUB;
+          if constexpr (T::FP8) {
+            // the E4M3 codes against the query's two E4M3 terms (columns [0, D/4) and
+            // [D/4, D/2) of Q), 32 codes a MMA, both into the same logits
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t bd = umma_desc(kbase + (kk >> 2) * T::KSLAB + (kk & 3) * 32, 16, 1024);
-            umma_f16_ta(t_sg, t_q + kk * 8, bd, ID_S, kk > 0);
+            for (int tm = 0; tm < 2; ++tm) {
+#pragma unroll
+              for (int kk = 0; kk < D / 32; ++kk) {
+                const uint64_t bd = umma_desc(kbase + kk * 32, 16, 1024);
+                umma_f8_ta(t_sg, t_q + tm * (D / 4) + kk * 8, bd, ID_S8, tm > 0 || kk > 0);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t bd = umma_desc(kbase + (kk >> 2) * T::KSLAB + (kk & 3) * 32, 16, 1024);
+              umma_f16_ta(t_sg, t_q + kk * 8, bd, ID_S, kk > 0);
+            }
           }
-          // the logits are ready; the K slot (or widened K buffer) of the step is free
+          // the logits are ready; the K slot of the step is free
           umma_commit(&s_full[g % NSP]);
-          if constexpr (T::FP8 && !T::CK_BY_S) umma_commit(&ck_free[g % T::NCK]);
-          if constexpr (!T::FP8 && !T::K_BY_S) umma_commit(&empty_k[g % T::NK]);
+          if constexpr (!T::K_BY_S) umma_commit(&empty_k[g % T::NK]);
           if (j >= LAG) issue_pv(g - LAG, j == LAG);
         }
         for (int j = nsub > LAG ? nsub - LAG : 0; j < nsub; ++j) issue_pv(g_item + j, j == 0);
@@ -776,26 +794,65 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       // rows of P and O are never read, and it keeps only the waits and arrivals that keep
       // the barriers' phases in step
       const bool warp_dead = __all_sync(kFull, !real);
-      // ---- this thread's query row into tensor memory, 16-bit pairs (every MMA of the
-      // previous item has completed); rows of no query are zero
-      {
-        const uint4* qrow = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const char*>(p.q) + ((((size_t)b * p.Sq + qi) * p.Hq + hq) * D) * 2);
+      // ---- this thread's query row into tensor memory (every MMA of the previous item has
+      // completed); rows of no query are zero
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const char*>(p.q) + ((((size_t)b * p.Sq + qi) * p.Hq + hq) * D) * 2);
+      float qk_row = qk_scale;  // the logit scale of this row
+      if constexpr (T::FP8) {
+        // fp8 cache: the row times a power of two sq (the largest with |q| sq <= 448) as two
+        // E4M3 terms, hi = e4m3(q sq) and lo = e4m3(q sq - hi), in columns [0, D/4) and
+        // [D/4, D/2), four codes a column; hi + lo holds q sq to about 2^-8 of its size (a
+        // 16-bit query's own precision is 2^-8 to 2^-11), the two MMAs of each 32 codes
+        // accumulate both into the logits, and 1/sq goes into the row's logit scale
+        auto q_f2 = [&](uint32_t w) { return QK == Q_BF16 ? bf16x2_to_f2(w) : f16x2_to_f2(w); };
+        float amax = 0.f;
+#pragma unroll 4
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = real ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int jw = 0; jw < 4; ++jw) {
+            const float2 f = q_f2(wv[jw]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+        }
+        int e = 0;  // floor(log2(448 / amax)), from the exponent field of the quotient
+        if (amax > 0.f) {
+          e = (int)((__float_as_uint(__fdiv_rn(448.f, amax)) >> 23) & 0xff) - 127;
+          e = max(-126, min(126, e));
+        }
+        const float sq = __uint_as_float((uint32_t)(e + 127) << 23);
+        qk_row = qk_scale * __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll 1
+        for (int h = 0; h < D / 64; ++h) {  // 64 dims: 16 columns of each term
+          uint32_t whi[16], wlo[16];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = real ? __ldg(qrow + 8 * h + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q4 = 0; q4 < 2; ++q4) {  // four dims, one column
+              const float2 fa = q_f2(wv[2 * q4]), fb = q_f2(wv[2 * q4 + 1]);
+              const float a0 = fa.x * sq, a1 = fa.y * sq, a2 = fb.x * sq, a3 = fb.y * sq;
+              const uint32_t h01 = f32x2_to_e4m3x2(a0, a1), h23 = f32x2_to_e4m3x2(a2, a3);
+              const float2 d01 = f16x2_to_f2(e4m3x2_to_h2(h01)), d23 = f16x2_to_f2(e4m3x2_to_h2(h23));
+              whi[2 * c + q4] = h01 | (h23 << 16);
+              wlo[2 * c + q4] = f32x2_to_e4m3x2(a0 - d01.x, a1 - d01.y) |
+                                (f32x2_to_e4m3x2(a2 - d23.x, a3 - d23.y) << 16);
+            }
+          }
+          tmem_st16u(t_q + lane_off + 16 * h, whi);
+          tmem_st16u(t_q + lane_off + D / 4 + 16 * h, wlo);
+        }
+        tmem_wait_st();
+      } else {
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
           uint32_t w[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            uint4 v = real ? __ldg(qrow + 8 * h + c) : make_uint4(0, 0, 0, 0);
-            if constexpr (T::FP8 && QK == Q_BF16) {  // f16 operands for an fp8 cache
-              uint32_t t4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int jw = 0; jw < 4; ++jw) {
-                const float2 f = bf16x2_to_f2(t4[jw]);
-                t4[jw] = pack16x2<false>(f.x, f.y);
-              }
-              v = make_uint4(t4[0], t4[1], t4[2], t4[3]);
-            }
+            const uint4 v = real ? __ldg(qrow + 8 * h + c) : make_uint4(0, 0, 0, 0);
             w[4 * c] = v.x;
             w[4 * c + 1] = v.y;
             w[4 * c + 2] = v.z;
@@ -859,7 +916,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
             tmem_ld32(t_sg + c0, x);
           }
           // ---- online softmax of this thread's logits (log2 units), two per instruction
-          const float2 s2 = make_float2(qk_scale, qk_scale), z2 = make_float2(0.f, 0.f);
+          const float2 s2 = make_float2(qk_row, qk_row), z2 = make_float2(0.f, 0.f);
           if constexpr (T::TOKS) {
             // logit j of the step times its key's scale
 #pragma unroll
@@ -1111,9 +1168,9 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   } else if (warp < T::W_CONV + T::NCW) {
     // ================================================================ fp8 widening
     if constexpr (T::FP8) {
-      // step g: the e4m3 K rows of ring slot g % NK become the f16 rows of K buffer
-      // g % NCK, then its V rows those of V buffer g % NSP (rows past the item's tokens
-      // become zero); the scales are applied to the logits and P, not here
+      // step g: the e4m3 V rows of ring slot g % NV become the f16 rows of V buffer g % NSP
+      // (rows past the item's tokens become zero); the scales are applied to the logits and
+      // P, not here, and the K codes go to the MMA as they are
       const int ctid = tid - T::W_CONV * 32;  // 0 .. 32 NCW - 1
       // one operand: 64 rows of 128 e4m3 codes -> two slabs of 64 rows of 64 f16 values.
       // Lane l of a warp takes 16-byte chunk l % 8 of a row, so each group of eight lanes
@@ -1157,29 +1214,14 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         const int nsub = ceil_div(t1 - t0, SUB);
         for (int j = 0; j < nsub; ++j, ++g) {
           const int nv = min(SUB, t1 - (t0 + j * SUB));
-          const int slot = (int)(g % T::NK), vslot = (int)(g % T::NV);
-          // ---- K rows (buffer g % NCK is free once the S of step g - NCK has completed)
-          wait_bar(&full_k[slot], (g / T::NK) & 1);
-          if (g >= (uint32_t)T::NCK) {
-            const uint32_t x = g - T::NCK;
-            if constexpr (T::CK_BY_S)
-              wait_bar(&s_full[x % NSP], (x / NSP) & 1);
-            else
-              wait_bar(&ck_free[x % T::NCK], (x / T::NCK) & 1);
-          }
-          widen(smem + T::OFF_K + slot * T::SLOT, smem + T::OFF_CV + (g % T::NCK) * T::CV_BUF, nv);
-          if (lane == 0) {
-            mbar_arrive(&ck_full[g % T::NCK]);
-            mbar_arrive(&empty_k[slot]);  // this warp is done with the K slot
-          }
+          const int vslot = (int)(g % T::NV);
           // ---- V rows (buffer g % NSP is free once the PV of step g - NSP has completed)
           wait_bar(&full_v[vslot], (g / T::NV) & 1);
           if (g >= (uint32_t)NSP) {
             const uint32_t x = g - NSP;
             wait_bar(&pv_done[x % NSP], (x / NSP) & 1);
           }
-          widen(smem + T::OFF_V + vslot * T::SLOT,
-                smem + T::OFF_CV + (T::NCK + g % NSP) * T::CV_BUF, nv);
+          widen(smem + T::OFF_V + vslot * T::SLOT, smem + T::OFF_CV + (g % NSP) * T::CV_BUF, nv);
           if (lane == 0) {
             mbar_arrive(&cv_full[g % NSP]);
             mbar_arrive(&empty_v[vslot]);

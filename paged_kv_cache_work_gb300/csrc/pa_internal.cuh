@@ -59,10 +59,8 @@ constexpr int kItemCostTiles = 3;
 // (head dim 128, bf16) and 9-10 us on the head-dim-256 Sq = 64 one, both about 430 tokens of
 // the CTA's own streaming (the query rows into tensor memory, the last PVs, the two token
 // streams' merge and the output or partial); seven steps balance the CTAs' exits there (the
-// long-context decode went from 37.5 to 35.0 us).  fp8 steps, slower per token, balanced at
-// six steps and measured slightly slower at seven.
+// long-context decode went from 37.5 to 35.0 us), and on the fp8 decodes too.
 constexpr int kTcItemCostSteps = 7;
-constexpr int kTcItemCostStepsFp8 = 6;
 
 inline int pow2_at_least(int x) {
   int p = 1;
@@ -119,9 +117,8 @@ inline Variant make_variant(const pa_config& c) {
   v.tt = v.path == 2 ? kTcStepTokens : kTileBytes / (c.head_dim * v.bpe);
   // the item cost is measured in 16 KB tiles of streaming (tcgen05: in steps), rounded up
   // to whole tiles
-  v.item_cost =
-      v.path == 2 ? (v.bpe == 1 ? kTcItemCostStepsFp8 : kTcItemCostSteps) * kTcStepTokens
-                  : round_up(kItemCostTiles * (kTileBytes / (c.head_dim * v.bpe)), v.tt);
+  v.item_cost = v.path == 2 ? kTcItemCostSteps * kTcStepTokens
+                            : round_up(kItemCostTiles * (kTileBytes / (c.head_dim * v.bpe)), v.tt);
   v.units = c.batch * c.num_kv_heads * v.rb;
   const int kvk = c.kv_dtype == PA_FP8_E4M3 ? 2 : (c.kv_dtype == PA_FP16 ? 1 : 0);
   const bool toks = c.kv_scale_mode == PA_SCALE_PER_TOKEN;

@@ -69,7 +69,6 @@ TILE_BYTES = 16384
 TC_STEP_TOKENS = 64
 ITEM_COST_TILES = 3
 TC_ITEM_COST_STEPS = 7
-TC_ITEM_COST_STEPS_FP8 = 6
 TC_MIN_ROWS = 33
 REDUCE_WARP_PIECES = 16
 
@@ -97,8 +96,7 @@ def variant(cfg: pa.PaConfig, ctas: int):
     cost = ITEM_COST_TILES * (TILE_BYTES // (cfg.head_dim * bpe))
     return dict(rows=rows, mp=mp, rb=rb, tt=tt, units=cfg.batch * cfg.num_kv_heads * rb,
                 ctas=ctas, ns_dec=decode_merge_limit(cfg.split_merge, tc),
-                item_cost=((TC_ITEM_COST_STEPS_FP8 if bpe == 1 else TC_ITEM_COST_STEPS) * TC_STEP_TOKENS
-                           if tc else -(-cost // tt) * tt))
+                item_cost=TC_ITEM_COST_STEPS * TC_STEP_TOKENS if tc else -(-cost // tt) * tt)
 
 
 def layout(cfg: pa.PaConfig, v: dict):
