@@ -26,8 +26,8 @@
 // 90 clocks more, and a wait for an MMA's completion right after issuing it drains the pipe
 // (measured on GB300 with standalone issue probes).  So every buffer is indexed by the step
 // modulo NSP, the number of S/P buffers, wherever shared memory allows: the commit that
-// tells the softmax its logits are ready also frees the step's K slot (or widened K
-// buffer), and the commit that ends a PV also frees its V slot: two commits per step.  And
+// tells the softmax its logits are ready also frees the step's K slot, and the commit that
+// ends a PV also frees its V slot (or widened V buffer): two commits per step.  And
 // the PV of step g trails its S by LAG = NSP - 2 steps where NSP >= 4, so the S that reuses
 // a buffer waits for a PV issued a step earlier, with MMAs still queued behind it.
 //
