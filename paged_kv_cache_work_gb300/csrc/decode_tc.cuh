@@ -114,7 +114,9 @@ struct TcTraits {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = D == 256 ? 256 : NSP * SUB;
   static constexpr uint32_t COL_Q = D == 256 ? NSP * SUB : COL_O + D;
-  static_assert(NSP * SUB + D + D / 2 <= (int)TMEM_COLS, "tensor memory");
+  // query columns: D / 2 16-bit pairs, or for an fp8 cache up to three E4M3 terms of D / 4
+  static constexpr int QCOLS = FP8 ? 3 * D / 4 : D / 2;
+  static_assert(NSP * SUB + D + QCOLS <= (int)TMEM_COLS, "tensor memory");
   static_assert(!TOKS || FP8, "per-token scales belong to fp8 caches");
   static_assert(!FP8 || D == 128, "fp8 caches at head dim 128");
   static_assert(!FP8 || (SUB * 8) % (32 * (NCW > 0 ? NCW : 1)) == 0, "widening: whole passes");
@@ -573,6 +575,9 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
   constexpr bool BF = KVK == KV_BF16;  // MMA operands bf16 (else f16: f16 and fp8 caches)
   constexpr uint32_t ID_S = umma_idesc(128, SUB, BF, false);
   constexpr uint32_t ID_S8 = umma_idesc(128, SUB, false, false);  // f8f6f4: E4M3 x E4M3
+  // E4M3 terms of a query row for an fp8 cache: a bf16 query's 8 significant bits fit in two
+  // of 4, an fp16 query's 11 in three
+  constexpr int QTERMS = QK == Q_BF16 ? 2 : 3;
   constexpr uint32_t ID_PV = umma_idesc(128, D, BF, true);
   constexpr int SOFT_BAR = 2;  // named barrier of the four softmax warps
   extern __shared__ char smem_raw[];
@@ -721,10 +726,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
           tc_fence_after();
           const uint32_t t_sg = t_s + (g % NSP) * SUB;
           if constexpr (T::FP8) {
-            // the E4M3 codes against the query's two E4M3 terms (columns [0, D/4) and
-            // [D/4, D/2) of Q), 32 codes a MMA, both into the same logits
+            // the E4M3 codes against the query's E4M3 terms (columns [t D/4, (t + 1) D/4) of
+            // Q for term t), 32 codes a MMA, all into the same logits
 #pragma unroll
-            for (int tm = 0; tm < 2; ++tm) {
+            for (int tm = 0; tm < QTERMS; ++tm) {
 #pragma unroll
               for (int kk = 0; kk < D / 32; ++kk) {
                 const uint64_t bd = umma_desc(kbase + kk * 32, 16, 1024);
@@ -800,11 +805,14 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
           reinterpret_cast<const char*>(p.q) + ((((size_t)b * p.Sq + qi) * p.Hq + hq) * D) * 2);
       float qk_row = qk_scale;  // the logit scale of this row
       if constexpr (T::FP8) {
-        // fp8 cache: the row times a power of two sq (the largest with |q| sq <= 448) as two
-        // E4M3 terms, hi = e4m3(q sq) and lo = e4m3(q sq - hi), in columns [0, D/4) and
-        // [D/4, D/2), four codes a column; hi + lo holds q sq to about 2^-8 of its size (a
-        // 16-bit query's own precision is 2^-8 to 2^-11), the two MMAs of each 32 codes
-        // accumulate both into the logits, and 1/sq goes into the row's logit scale
+        // fp8 cache: the row times a power of two sq (the largest with |q| sq <= 448) as
+        // QTERMS E4M3 terms, t0 = e4m3(q sq), t1 = e4m3(q sq - t0), t2 = e4m3(q sq - t0 - t1),
+        // term t in columns [t D/4, (t + 1) D/4), four codes a column.  Each term carries the
+        // next 4 significant bits, so the terms sum to the query exactly (two for bf16's 8
+        // bits, three for fp16's 11) but for elements whose low bits fall below the smallest
+        // E4M3 subnormal, about a thousandth of the row's largest and smaller; the MMAs of
+        // each 32 codes accumulate all terms into the logits, and 1/sq goes into the row's
+        // logit scale
         auto q_f2 = [&](uint32_t w) { return QK == Q_BF16 ? bf16x2_to_f2(w) : f16x2_to_f2(w); };
         float amax = 0.f;
 #pragma unroll 4
@@ -826,7 +834,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         qk_row = qk_scale * __uint_as_float((uint32_t)(127 - e) << 23);
 #pragma unroll 1
         for (int h = 0; h < D / 64; ++h) {  // 64 dims: 16 columns of each term
-          uint32_t whi[16], wlo[16];
+          uint32_t wt[QTERMS][16];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 v = real ? __ldg(qrow + 8 * h + c) : make_uint4(0, 0, 0, 0);
@@ -834,16 +842,25 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {  // four dims, one column
               const float2 fa = q_f2(wv[2 * q4]), fb = q_f2(wv[2 * q4 + 1]);
-              const float a0 = fa.x * sq, a1 = fa.y * sq, a2 = fb.x * sq, a3 = fb.y * sq;
-              const uint32_t h01 = f32x2_to_e4m3x2(a0, a1), h23 = f32x2_to_e4m3x2(a2, a3);
-              const float2 d01 = f16x2_to_f2(e4m3x2_to_h2(h01)), d23 = f16x2_to_f2(e4m3x2_to_h2(h23));
-              whi[2 * c + q4] = h01 | (h23 << 16);
-              wlo[2 * c + q4] = f32x2_to_e4m3x2(a0 - d01.x, a1 - d01.y) |
-                                (f32x2_to_e4m3x2(a2 - d23.x, a3 - d23.y) << 16);
+              // what is left of the four scaled elements after the terms so far (exact)
+              float r0 = fa.x * sq, r1 = fa.y * sq, r2 = fb.x * sq, r3 = fb.y * sq;
+#pragma unroll
+              for (int tm = 0; tm < QTERMS; ++tm) {
+                const uint32_t c01 = f32x2_to_e4m3x2(r0, r1), c23 = f32x2_to_e4m3x2(r2, r3);
+                wt[tm][2 * c + q4] = c01 | (c23 << 16);
+                if (tm + 1 < QTERMS) {
+                  const float2 d01 = f16x2_to_f2(e4m3x2_to_h2(c01));
+                  const float2 d23 = f16x2_to_f2(e4m3x2_to_h2(c23));
+                  r0 -= d01.x;
+                  r1 -= d01.y;
+                  r2 -= d23.x;
+                  r3 -= d23.y;
+                }
+              }
             }
           }
-          tmem_st16u(t_q + lane_off + 16 * h, whi);
-          tmem_st16u(t_q + lane_off + D / 4 + 16 * h, wlo);
+#pragma unroll
+          for (int tm = 0; tm < QTERMS; ++tm) tmem_st16u(t_q + lane_off + tm * (D / 4) + 16 * h, wt[tm]);
         }
         tmem_wait_st();
       } else {

@@ -79,3 +79,45 @@ def test_every_code_widens_exactly(heads, scale_mode, cuda_device, pa):
     ok = ~nan_want
     bad = np.nonzero(got[ok] != want[ok])[0]
     assert bad.size == 0, f"{bad.size} elements differ, e.g. {got[ok][bad[:4]]} vs {want[ok][bad[:4]]}"
+
+
+def shaped_queries(q: torch.Tensor, seed: int) -> torch.Tensor:
+    """Query rows whose magnitudes stress a kernel that rescales and splits a row: elements
+    spread over six orders of magnitude, an all-zero row, a row of large values, a row of
+    tiny ones (subnormal in fp16), and a row with one outlier; the rest N(0, 1)."""
+    g = torch.Generator().manual_seed(seed)
+    B, Sq, Hq, D_ = q.shape
+    x = torch.randn((B, Sq, Hq, D_), generator=g, dtype=torch.float64)
+    kind = torch.arange(B * Sq * Hq).reshape(B, Sq, Hq) % 6
+    spread = 10.0 ** (torch.rand((B, Sq, Hq, D_), generator=g, dtype=torch.float64) * 6 - 3)
+    x = torch.where((kind == 0)[..., None], x * spread, x)
+    x = torch.where((kind == 1)[..., None], torch.zeros_like(x), x)
+    x = torch.where((kind == 2)[..., None], x * 30.0, x)
+    x = torch.where((kind == 3)[..., None], x * 1e-5, x)
+    outlier = torch.zeros_like(x)
+    outlier[..., 7] = 300.0
+    x = torch.where((kind == 4)[..., None], x + outlier, x)
+    return x.to(q.dtype)
+
+
+RANGE_CASES = [("tcgen05", 16, "bf16", "tensor"), ("tcgen05", 16, "fp16", "token"),
+               ("tcgen05", 16, "fp16", "none"), ("mma", 4, "fp16", "tensor")]
+
+
+@pytest.mark.parametrize("kernel,heads,q_dtype,scale_mode", RANGE_CASES,
+                         ids=[f"{k}_{q}_{m}" for k, _, q, m in RANGE_CASES])
+def test_query_dynamic_range(kernel, heads, q_dtype, scale_mode, cuda_device, pa):
+    """Rows of very different magnitudes against an fp8 cache, compared with the oracle at
+    the fp8 tolerance (64 query rows per kv head take the tcgen05 kernel, 16 the mma.sync
+    one)."""
+    from pagedkv import random_problem
+    from gpu_run import compare
+    rng = np.random.default_rng(77 + heads)
+    inp, _ = random_problem(rng, batch=3, max_q_len=4, num_q_heads=heads, num_kv_heads=1,
+                            head_dim=D, block_size=64, ctx=[300, 77, 700], q_dtype=q_dtype,
+                            kv_dtype="fp8", scale_mode=scale_mode, causal=True)
+    inp["q"] = shaped_queries(inp["q"], 5)
+    ref_out, ref_lse = oracle.decode(inp, "f32")
+    out, lse, ws, _ = run(W.to_device(inp, cuda_device))
+    assert pa.read_flags(ws) == 0
+    compare(out, lse, ref_out, ref_lse, "fp8")
