@@ -75,6 +75,11 @@ struct TcTraits {
   static constexpr int NK = D == 256 && !FP8 ? 3 : NSP;    // K ring slots
   static constexpr int NV = FP8 ? 5 : (D == 256 ? 3 : NSP);  // V ring slots
   static constexpr bool K_BY_S = NK == NSP;            // a K slot is released by its S's commit
+  // steps the copy warp issues K ahead of V: for fp8 the V slots wait for the widening, which
+  // waits for the PV of four steps back, and K copies held behind them left the logits MMA
+  // waiting for its codes (per-tensor fp8 Sq = 4: 76.6 -> 76.0 us).  With per-token scales,
+  // which go out with K, the longer lead measured slower.
+  static constexpr int KLEAD = FP8 && !TOKS ? 2 : 1;
   static constexpr bool V_BY_PV = !FP8 && NV == NSP;  // a V slot is released by its PV's commit
   static constexpr int ROWB = 128;             // swizzled slabs of 128 bytes per row
   static constexpr int NSLAB = D * BPE / 128;  // slabs of a cache tile row
@@ -537,16 +542,35 @@ struct TcProducer {
   }
 
   __device__ __forceinline__ void run() {
-    Box cur, nxt;
-    if (!next_tile(cur)) return;
-    if (!issue_k(cur)) return;
-    while (true) {
-      const bool more = next_tile(nxt);
-      if (more && !issue_k(nxt)) return;
-      if (!issue<T::NV>(cur, nv, full_v, rel_v, vmap, T::OFF_V)) return;
+    // K runs KLEAD steps ahead of V: q[0 .. pending) are the tiles whose K is out and whose
+    // V is not yet, oldest first (fixed indices, shifted down after each V, so that they
+    // stay in registers)
+    constexpr int KLEAD = T::KLEAD;
+    Box q[KLEAD + 1];
+    int pending = 0;
+    bool more = true;
+#pragma unroll
+    for (int i = 0; i < KLEAD; ++i) {
+      if (more) more = next_tile(q[i]);
+      if (more) {
+        if (!issue_k(q[i])) return;
+        pending = i + 1;
+      }
+    }
+    while (pending > 0) {
+      bool added = false;
+      if (more && pending == KLEAD) {  // steady state: one tile in, one out
+        more = next_tile(q[KLEAD]);
+        if (more) {
+          if (!issue_k(q[KLEAD])) return;
+          added = true;
+        }
+      }
+      if (!issue<T::NV>(q[0], nv, full_v, rel_v, vmap, T::OFF_V)) return;
       ++nv;
-      if (!more) return;
-      cur = nxt;
+#pragma unroll
+      for (int i = 0; i < KLEAD; ++i) q[i] = q[i + 1];
+      if (!added) --pending;
     }
   }
 
