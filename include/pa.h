@@ -102,7 +102,9 @@ enum {
   PA_FLAG_BAD_LENGTHS = 1,   /* q_lens[b] outside [0, max_q_len], context_lens[b] < q_lens[b],
                                 or context_lens[b] > max_blocks_per_seq * block_size */
   PA_FLAG_BAD_BLOCK_ID = 2,  /* a block_tables entry in use lies outside [0, num_blocks) */
-  PA_FLAG_WAIT_TIMEOUT = 4   /* a kernel gave up a bounded wait on its own copies */
+  PA_FLAG_WAIT_TIMEOUT = 4,  /* a kernel gave up a bounded wait on its own copies */
+  PA_FLAG_STALE_PLAN = 8     /* pa_decode read lengths other than those pa_plan planned for
+                                (they changed between the two calls); outputs unspecified */
 };
 
 typedef struct {
@@ -148,8 +150,18 @@ PA_API pa_status pa_plan(const pa_config *cfg, const int32_t *block_tables, cons
  *   out      [B, Sq, Hq, D]            q_dtype; written for every unit done in one piece,
  *            with no keys, or merged here (see pa_split_merge)
  *   lse      [B, Sq, Hq] fp32 natural-log LSE, or NULL
- * The tables and lengths must be the ones given to pa_plan.  A decode that completed leaves
- * the merge counters as pa_plan set them, so pa_decode may run again on the same plan. */
+ * The tables and lengths must be the ones given to pa_plan, with the same contents.  A CTA
+ * of the tcgen05 decode (33 or more query rows per kv head; head dim 128 or 256, 128 for an
+ * fp8 cache) derives its first work item from the lengths (the planner's rules) and starts
+ * on it while the planner may still be running; it waits for the planner before the rest of
+ * its list and before writing anything, and raises PA_FLAG_STALE_PLAN if the planner's first
+ * item differs.  The other decode kernels wait for the planner first.
+ * The kernels launch with programmatic dependent launch, so pa_decode reads q, the caches,
+ * the tables and the lengths once the launch before it in the stream has let its dependents
+ * start (a pa_plan call does so after its own wait on the launch before it): a kernel between
+ * pa_plan and pa_decode that writes any of them must not let its dependents start early.
+ * A decode that completed leaves the merge counters as pa_plan set them, so pa_decode may
+ * run again on the same plan. */
 PA_API pa_status pa_decode(const pa_config *cfg, const void *q, const void *k_cache, const void *v_cache,
                     const float *k_scale, const float *v_scale, const int32_t *block_tables,
                     const int32_t *context_lens, const int32_t *q_lens, void *out, float *lse,

@@ -18,7 +18,8 @@ __all__ = ["PaConfig", "PaError", "load", "workspace_size", "plan", "decode", "r
            "decode_step_static", "STATIC_SCRATCH_BYTES", "append_kv", "gather_kv",
            "read_flags", "status_string", "config_for", "paged_attention", "LIB_PATH",
            "BF16", "FP16", "FP8_E4M3", "SCALE_NONE", "SCALE_PER_TENSOR", "SCALE_PER_TOKEN",
-           "FLAG_BAD_LENGTHS", "FLAG_BAD_BLOCK_ID", "FLAG_WAIT_TIMEOUT", "EXPORTED_SYMBOLS",
+           "FLAG_BAD_LENGTHS", "FLAG_BAD_BLOCK_ID", "FLAG_WAIT_TIMEOUT", "FLAG_STALE_PLAN",
+           "EXPORTED_SYMBOLS",
            "MERGE_AUTO", "MERGE_IN_DECODE", "MERGE_IN_REDUCE"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +30,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = rang
 # pa_dtype, pa_scale_mode, flags
 BF16, FP16, FP8_E4M3 = 0, 1, 2
 SCALE_NONE, SCALE_PER_TENSOR, SCALE_PER_TOKEN = 0, 1, 2
-FLAG_BAD_LENGTHS, FLAG_BAD_BLOCK_ID, FLAG_WAIT_TIMEOUT = 1, 2, 4
+FLAG_BAD_LENGTHS, FLAG_BAD_BLOCK_ID, FLAG_WAIT_TIMEOUT, FLAG_STALE_PLAN = 1, 2, 4, 8
 MERGE_AUTO, MERGE_IN_DECODE, MERGE_IN_REDUCE = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("pa_workspace_size", "pa_plan", "pa_decode", "pa_reduce", "pa_read_flags",

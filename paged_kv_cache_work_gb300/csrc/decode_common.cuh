@@ -37,7 +37,75 @@ struct KernelParams {
   int Sq, Hq, Hkv, G, M, RB, bs, maxb, nblocks, causal;
   int bs_shift;  // log2(bs): pages are a power of two
   float qk_scale;
+  // the planner's inputs, for a CTA that derives its own first work item (first_item_of)
+  int batch, tt, tt_shift, item_cost;
 };
+
+// The first work item of CTA c of C, derived from the lengths with the planner's own rules
+// and integer arithmetic (the concatenated token space of plan.cu: each unit its tile-padded
+// length plus the item cost, cut into C equal tile-aligned pieces), so that a CTA can start
+// on it before the planner has finished.  One whole warp: one pass sums the space (any bad
+// length gives no items, as in the planner), a second finds the sequence holding the
+// piece's first position with a running warp scan.  Returns (0, 0, 0, -1) when the CTA has
+// no items.
+static __device__ __noinline__ int4 first_item_of(const KernelParams& p, int c, int C, int lane) {
+  const int4 none = make_int4(0, 0, 0, -1);
+  const int ups = p.Hkv * p.RB;
+  const long long cap = (long long)p.maxb * p.bs;
+  auto pad = [&](int len) { return ((len + p.tt - 1) >> p.tt_shift) << p.tt_shift; };
+  auto stride = [&](int len) { return len > 0 ? pad(len) + p.item_cost : 0; };
+  int total = 0;
+  bool bad = false;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    if (b < p.batch) {
+      const int n = __ldg(p.ctx + b), ql = __ldg(p.qlens + b);
+      if (ql < 0 || ql > p.Sq || n < ql || (long long)n > cap)
+        bad = true;
+      else
+        total += stride(n) * ups;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
+  if (__any_sync(kFull, bad) || total <= 0) return none;
+  const int T = total;
+  const int chunk = pad((int)(((uint32_t)T + (uint32_t)C - 1u) / (uint32_t)C));
+  if (c >= (T - 1) / chunk + 1) return none;  // past the active CTAs
+  const int lo = c * chunk, hi = min(lo + chunk, T) - 1;
+  // the last sequence whose start is <= lo (a sequence with no tokens shares its
+  // successor's start, so the last one is never empty)
+  int run = 0, start_f = 0, n_f = 0, b_f = 0;
+  for (int b0 = 0; b0 < p.batch && run <= lo; b0 += 32) {
+    const int b = b0 + lane;
+    const int n = b < p.batch ? __ldg(p.ctx + b) : 0;
+    const int span = stride(n) * ups;
+    int x = span;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    const int start = run + x - span;
+    const unsigned m = __ballot_sync(kFull, b < p.batch && start <= lo);
+    if (m) {
+      const int l = 31 - __clz(m);
+      b_f = b0 + l;
+      start_f = __shfl_sync(kFull, start, l);
+      n_f = __shfl_sync(kFull, n, l);
+    }
+    run += __shfl_sync(kFull, x, 31);
+  }
+  const int pf = stride(n_f);
+  const int ku = (lo - start_f) / pf;
+  const int st = start_f + ku * pf;
+  int t0 = max(lo, st) - st, t1 = min(hi + 1 - st, n_f), slot = -1;
+  if (t1 <= t0)
+    t0 = t1 = 0;  // only the item-cost stretch of the unit lies in this piece
+  else if (st < lo || st + pad(n_f) - 1 > hi)
+    slot = 2 * c;  // the unit's tiles reach out of this piece
+  return make_int4(b_f * ups + ku, t0, t1, slot);
+}
 
 // ---- element conversion -----------------------------------------------------------
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {

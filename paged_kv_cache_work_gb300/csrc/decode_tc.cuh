@@ -109,7 +109,8 @@ struct TcTraits {
   // o_free, q_full, mma_end, cv_full (NCV), sc_full and
   // sc_free (NSC each)
   static constexpr int NBAR = 2 * NK + 2 * NV + 3 * NSP + 3 + NCV + 2 * NSC;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 16 + 1024;
+  // after the barriers: the flag words, the derived first item and the CTA's flags
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + kFlagBytes + 32 + 1024;
   static constexpr int CTAS_PER_SM = 1;
   // Tensor memory (lane = query row, 32-bit columns): NSP S/P buffers of SUB fp32 columns
   // (P, SUB / 2 columns of 16-bit pairs, overwrites the first half of its own S), O (D fp32
@@ -350,6 +351,49 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 // on memory: the parameters it uses live in registers, and each lane's block id is looked
 // up two tiles before its copy is issued (and not at all while the tile stays on the page of
 // the previous one).
+// A CTA's work list as one thread sees it: item 0 is the one the CTA derived from the lengths
+// (first_item_of); the rest are the planner's, items [lb + 1, le) of its list, read after
+// the first wait on the planner, which also lets the next launch start (so the next launch
+// starts only once the planner has finished: the reduce kernel reads the planner's list
+// before its own wait on this grid).
+struct ItemList {
+  const int32_t* item_off;
+  const int4* items;
+  int4 first;
+  int lb, le;  // le < 0 until the planner's list has been read
+
+  __device__ __forceinline__ void init(const KernelParams& p, int4 f) {
+    item_off = p.item_off;
+    items = p.items;
+    first = f;
+    lb = 0;
+    le = -1;
+  }
+  // wait for the planner (a no-op once it has finished for this thread)
+  __device__ __forceinline__ void wait_planner() {
+    grid_dependency_wait();
+    grid_dependents_launch();
+  }
+  // wait for the planner (once) and read the CTA's range of its list
+  __device__ __forceinline__ void planned() {
+    if (le >= 0) return;
+    wait_planner();
+    lb = item_off[blockIdx.x];
+    le = item_off[blockIdx.x + 1];
+  }
+  // item k (k >= 1 waits for the planner); false past the list's end
+  __device__ __forceinline__ bool get(int k, int4& item) {
+    if (k == 0) {
+      item = first;
+      return true;
+    }
+    planned();
+    if (lb + k >= le) return false;
+    item = items[lb + k];
+    return true;
+  }
+};
+
 template <class T>
 struct TcProducer {
   struct Box {
@@ -367,7 +411,7 @@ struct TcProducer {
   char* smem;
   uint64_t *full_k, *rel_k, *full_v, *rel_v, *sc_full, *sc_free;
   volatile int* abort_flag;
-  int32_t* flags;
+  int* flags;  // the CTA's flags in shared memory, published once the planner has finished
   const int32_t* bt;
   const int4* items;
   const float* kscale;
@@ -377,20 +421,21 @@ struct TcProducer {
   uint32_t box_bytes, nk, nv, nsc;
   bool scale_bulk;  // a tile's scales are two contiguous 256-byte runs (one kv head, big pages)
   // walk over the work list (the tile after the two being fetched)
-  int it, it_end, k, ntiles, t0, t1, b, g;
+  ItemList list;
+  int it, k, ntiles, t0, t1, b, g;
   bool have;
-  int4 item_next;
+  int4 item_next;  // item it + 1 once past item 0
   int last_b, last_page, last_blk;  // this lane's previous lookup
   Ahead q0, q1;
 
   __device__ __forceinline__ void init(const KernelParams* prm, const CUtensorMap* km,
                                        const CUtensorMap* vm, char* sm, uint64_t* fk,
                                        uint64_t* rk, uint64_t* fv, uint64_t* rv, uint64_t* scf,
-                                       uint64_t* scr, volatile int* ab, int ln, int ib, int ie,
+                                       uint64_t* scr, volatile int* ab, int* sflags, int ln,
                                        int4 first) {
     kmap = km; vmap = vm; smem = sm; full_k = fk; rel_k = rk; full_v = fv; rel_v = rv;
     sc_full = scf; sc_free = scr; abort_flag = ab; lane = ln;
-    flags = prm->flags; bt = prm->bt; items = prm->items; kscale = prm->k_scale;
+    flags = sflags; bt = prm->bt; items = prm->items; kscale = prm->k_scale;
     vscale = prm->v_scale; maxb = prm->maxb; bs = prm->bs; bs_shift = prm->bs_shift;
     nblocks = prm->nblocks; Hkv = prm->Hkv; RB = prm->RB;
     box_rows = min(bs, T::TT);
@@ -399,10 +444,9 @@ struct TcProducer {
     scale_bulk = T::TOKS && Hkv == 1 && box_rows == T::TT &&
                  ((reinterpret_cast<uintptr_t>(kscale) | reinterpret_cast<uintptr_t>(vscale)) & 15) == 0;
     nk = nv = nsc = 0;
-    it = ib - 1;
-    it_end = ie;
+    list.init(*prm, first);
+    it = -1;
     have = false;
-    item_next = first;  // item ib, or (0, 0, 0, -1)
     last_b = -1;
     last_page = -1;
     last_blk = -1;
@@ -413,12 +457,22 @@ struct TcProducer {
   // The next tile of the work list into a, with this lane's block id lookup started.
   __device__ __forceinline__ void fetch(Ahead& a) {
     while (!have) {
-      if (++it >= it_end) {
-        a.valid = false;
-        return;
+      int4 item;
+      if (++it == 0) {
+        item = list.first;
+      } else {
+        // item it, read one ahead from item 1 on (item 0 needs no list: no wait for it)
+        if (it == 1 && !list.get(1, item_next)) {
+          a.valid = false;
+          return;
+        }
+        if (list.lb + it >= list.le) {
+          a.valid = false;
+          return;
+        }
+        item = item_next;
+        if (!list.get(it + 1, item_next)) item_next = make_int4(0, 0, 0, -1);
       }
-      const int4 item = item_next;
-      if (it + 1 < it_end) item_next = items[it + 1];
       t0 = item.y;
       t1 = item.z;
       if (t1 <= t0) continue;
@@ -654,6 +708,8 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     *abort_flag = 0;
     pend[0] = -1;
     pend[2] = -1;
+    abort_flag[12] = 0;  // the CTA's flags (s_flags)
+    abort_flag[13] = 0;  // 1 once the derived first item is checked against the planner's
     fence_barrier_init();
   }
   if (warp == T::W_MMA) {
@@ -666,22 +722,40 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
   }
+  // The CTA's first work item, derived from the lengths (the planner's rules), so that its
+  // copies and MMAs start while the planner may still be running.  The lengths, the tables,
+  // the queries and the caches were written before the planner ran (this grid starts only
+  // once the planner has passed its own wait), so they may be read now; the planner's list
+  // and every write wait for the planner (ItemList::planned).
+  volatile int* s_first = abort_flag + 8;  // 4 ints
+  if (warp == T::W_SOFT) {
+    const int4 f = first_item_of(p, blockIdx.x, gridDim.x, lane);
+    if (lane == 0) {
+      s_first[0] = f.x;
+      s_first[1] = f.y;
+      s_first[2] = f.z;
+      s_first[3] = f.w;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t t_s = tmem, t_o = tmem + T::COL_O, t_q = tmem + T::COL_Q;
-  grid_dependency_wait();  // the work list comes from the planner launched just before
-  // the next kernel may start launching now: it is held in its own grid_dependency_wait
-  // until this grid has completed, and it cannot take the place of a CTA of this grid
-  grid_dependents_launch();
-
-  // the CTA's item range and its first item, read together (one round trip)
-  const int it_begin = p.item_off[blockIdx.x], it_end = p.item_off[blockIdx.x + 1];
-  const int4 first = p.first_item[blockIdx.x];
+  const int4 first = make_int4(s_first[0], s_first[1], s_first[2], s_first[3]);
+  // flags raised before the planner's own header write could be overwritten by it: they are
+  // gathered here and published at the end
+  int* s_flags = const_cast<int*>(abort_flag + 12);
+  volatile int* first_checked = abort_flag + 13;
+  // the item this CTA derived must be the planner's (else the lengths changed between the
+  // planner's launch and this one)
+  auto check_first = [&](int4 pf) {
+    if (pf.x != first.x || pf.y != first.y || pf.z != first.z || pf.w != first.w)
+      atomicOr(s_flags, PA_FLAG_STALE_PLAN);
+  };
   auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
     if (!mbar_wait(bar, parity, abort_flag)) {
-      atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
+      atomicOr(s_flags, PA_FLAG_WAIT_TIMEOUT);
       *abort_flag = 1;
     }
   };
@@ -690,8 +764,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     // ================================================================ TMA producer
     TcProducer<T> prod;
     prod.init(&p, &kmap, &vmap, smem, full_k, T::K_BY_S ? s_full : empty_k, full_v,
-              T::V_BY_PV ? pv_done : empty_v, sc_full, sc_free, abort_flag, lane, it_begin,
-              it_end, first);
+              T::V_BY_PV ? pv_done : empty_v, sc_full, sc_free, abort_flag, s_flags, lane, first);
     prod.run();  // every tile of the work list, as slots come free
     prod.drain();
   } else if (warp == T::W_MMA) {
@@ -727,8 +800,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         umma_commit(&pv_done[gp % NSP]);
         if constexpr (!T::FP8 && !T::V_BY_PV) umma_commit(&empty_v[gp % T::NV]);
       };
-      for (int it = it_begin; it < it_end; ++it) {
-        const int4 item = it == it_begin ? first : p.items[it];
+      ItemList list;
+      list.init(p, first);
+      int4 item;
+      for (int it = 0; list.get(it, item); ++it) {
         const int t0 = item.y, t1 = item.z;
         if (t1 <= t0) continue;
         const int nsub = ceil_div(t1 - t0, SUB);
@@ -776,7 +851,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         ++items_done;
       }
       umma_commit(mma_end);
-      if (!mbar_wait_drain(mma_end, 0)) atomicOr(p.flags, PA_FLAG_WAIT_TIMEOUT);
+      if (!mbar_wait_drain(mma_end, 0)) atomicOr(s_flags, PA_FLAG_WAIT_TIMEOUT);
     }
   } else if (warp < T::W_CONV) {
     // ================================================================ softmax and epilogue
@@ -803,16 +878,41 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       tc_fence_after();
     };
     int2 pend_even = make_int2(-1, 0), pend_odd = make_int2(-1, 0);  // held by stid 0
-    int4 item_next = first;
-    for (int it = it_begin; it < it_end; ++it) {
-      const int4 item = item_next;
-      if (it + 1 < it_end) item_next = p.items[it + 1];
+    ItemList list;
+    list.init(p, first);
+    int4 item, item_next;
+    bool have_next = false;
+    for (int it = 0;; ++it) {
+      if (it == 0)
+        item = first;
+      else if (have_next)
+        item = item_next;
+      else if (!list.get(it, item))
+        break;
+      // the next item is read ahead from item 1 on (item 0 waits for nothing)
+      have_next = it >= 1 && list.get(it + 1, item_next);
       const int u = item.x, t0 = item.y, t1 = item.z, slot = item.w;
       if (t1 <= t0) continue;
       const int b = u / (p.Hkv * p.RB), g_kv = (u / p.RB) % p.Hkv, rb = u % p.RB;
       const int n = __ldg(p.ctx + b), ql = __ldg(p.qlens + b);
-      const int2 uinfo = slot >= 0 ? __ldg(&p.unit_info[u]) : make_int2(0, 1);
-      const bool in_dec = slot >= 0 && uinfo.y <= p.ns_dec;
+      // the unit's pieces (planner data): for item 0 read halfway through it, when the
+      // planner has long finished, off the path of its last steps
+      int2 uinfo = make_int2(0, 1);
+      bool in_dec = false;
+      auto read_uinfo = [&]() {
+        list.wait_planner();
+        int4 pf = first;
+        if (it == 0 && stid == 0) pf = p.first_item[blockIdx.x];
+        if (slot >= 0) {
+          uinfo = __ldg(&p.unit_info[u]);
+          in_dec = uinfo.y <= p.ns_dec;
+        }
+        if (it == 0 && stid == 0) {
+          check_first(pf);
+          first_checked[0] = 1;
+        }
+      };
+      if (it > 0) read_uinfo();
       const int nsub = ceil_div(t1 - t0, SUB);
       int cnt_seen = -1;
       const int rg = rb * MP + qr;
@@ -911,6 +1011,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       for (int j = 0; j < nsub; ++j, ++g) {
         const int tok0 = t0 + j * SUB, nv = min(SUB, t1 - tok0);  // tokens of the item here
         const int c0 = NL * hs;  // this stream's first token of the step
+        if (it == 0 && j == (nsub - 1) / 2) read_uinfo();
         if (in_dec && j + 1 == nsub && stid == 0) cnt_seen = ld_acquire_gpu(&p.unit_cnt[u]);
         if (!T::FP8 && nv < SUB) {
           // the zeroing below writes into the V slot: the tile must have landed (this wait
@@ -1072,6 +1173,7 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         }
       }
       // ---- epilogue: O of this thread's row from tensor memory, in two halves of 64 dims
+      list.wait_planner();  // nothing is written before the planner has finished
       wait_pv_step(g - 1);  // every PV of the item (in order)
       if (stid == 0) *cnt_seen_s = cnt_seen;
       named_barrier_sync(SOFT_BAR, 128);
@@ -1248,8 +1350,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
         __syncwarp();
       };
       uint32_t g = 0;
-      for (int it = it_begin; it < it_end; ++it) {
-        const int4 item = it == it_begin ? first : p.items[it];
+      ItemList list;
+      list.init(p, first);
+      int4 item;
+      for (int it = 0; list.get(it, item); ++it) {
         const int t0 = item.y, t1 = item.z;
         if (t1 <= t0) continue;
         const int nsub = ceil_div(t1 - t0, SUB);
@@ -1272,6 +1376,10 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     }
   }
 
+  // every thread past the planner (a role may have needed none of its list) before the
+  // writes below
+  grid_dependency_wait();
+  grid_dependents_launch();
   tc_fence_before();
   __syncthreads();  // every role is done: no copy or MMA in flight
   if (warp >= T::W_SOFT && warp < T::W_CONV) {
@@ -1280,6 +1388,11 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
     zero_empty_units<D, MP, QK, 128>(p, stid);
   }
   __syncthreads();
+  if (tid == 0) {
+    // a CTA whose first item was empty or absent checks it here
+    if (*first_checked == 0) check_first(p.first_item[blockIdx.x]);
+    if (*s_flags != 0) atomicOr(p.flags, *s_flags);
+  }
   if (warp == T::W_MMA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),

@@ -84,6 +84,10 @@ KernelParams make_kernel_params(const DecodeArgs& a) {
   p.nblocks = a.p.num_blocks;
   p.causal = a.p.causal;
   p.qk_scale = a.qk_scale;
+  p.batch = a.p.batch;
+  p.tt = a.v.tt;
+  p.tt_shift = ilog2((uint32_t)a.v.tt);
+  p.item_cost = a.v.item_cost;
   return p;
 }
 

@@ -78,3 +78,23 @@ def test_flags_reset_by_next_plan(cuda_device):
     inp["q_lens"] = good_q
     pa.paged_attention(inp, ws=ws, cfg=cfg)
     assert pa.read_flags(ws) == 0
+
+
+def test_lengths_changed_after_planning(cuda_device):
+    """The tcgen05 decode derives each CTA's first work item from the lengths and checks it
+    against the planner's: lengths changed between pa_plan and pa_decode (shorter, so every
+    key the changed plan reaches is still inside its sequence's pages) raise
+    PA_FLAG_STALE_PLAN, and nothing is read outside the inputs."""
+    wl = W.reduced(W.LONG_SQ4, 3, 3000, 6000)  # 64 query rows per kv head: tcgen05
+    inp = W.make_inputs(wl, 2026, device=cuda_device)
+    cfg = pa.config_for(inp)
+    q = inp["q"]
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=cuda_device)
+    ws = torch.empty(pa.workspace_size(cfg), dtype=torch.uint8, device=cuda_device)
+    pa.plan(cfg, inp["block_tables"], inp["context_lens"], inp["q_lens"], ws)
+    ctx = (inp["context_lens"] // 2).clone()
+    pa.decode(cfg, q, inp["k_cache"], inp["v_cache"], None, None, inp["block_tables"], ctx,
+              inp["q_lens"], out, lse, ws)
+    torch.cuda.synchronize()
+    assert pa.read_flags(ws) & pa.FLAG_STALE_PLAN

@@ -101,6 +101,8 @@ CASES = [
     ("long_sq4", W.reduced(W.LONG_SQ4, 3, 4, 20000), [152, 3]),
     ("mha_sq16", W.reduced(W.mha_d256(8, 16), 3, 16, 4000), [152, 64]),
     ("fp8_token", W.reduced(W.FP8_TOKEN_SQ1, 5, 1, 5000), [152, 9]),
+    # a tcgen05 decode's planner keeps prefix sums of at most 1024 sequences in shared memory
+    ("long_sq4_many_sequences", W.reduced(W.LONG_SQ4, 1100, 4, 300), [152]),
 ]
 
 
