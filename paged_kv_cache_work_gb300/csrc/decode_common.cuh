@@ -48,7 +48,7 @@ struct KernelParams {
 // length gives no items, as in the planner), a second finds the sequence holding the
 // piece's first position with a running warp scan.  Returns (0, 0, 0, -1) when the CTA has
 // no items.
-static __device__ __noinline__ int4 first_item_of(const KernelParams& p, int c, int C, int lane) {
+static __device__ __forceinline__ int4 first_item_of(const KernelParams& p, int c, int C, int lane) {
   const int4 none = make_int4(0, 0, 0, -1);
   const int ups = p.Hkv * p.RB;
   const long long cap = (long long)p.maxb * p.bs;
