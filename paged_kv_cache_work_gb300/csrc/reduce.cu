@@ -130,6 +130,8 @@ struct ReduceParams {
   const float* o_part;
   const float* lse_part;
   int Sq, Hq, Hkv, G, M, RB, MP;
+  int R;  // rows of a unit in the row space: M when a unit is one row block (the tile's
+          // padding rows are left out), else MP (only the last block has padding rows)
 };
 
 constexpr int kReduceWarps = 8;
@@ -138,71 +140,91 @@ constexpr int kReduceWarps = 8;
 // kReduceWarpPieces pieces, then the rest.
 //  * Few pieces: one warp per (unit, row), lanes over the head dimension (four floats a
 //    lane); lane s holds piece s's log2-sum-exp, so the row's max and weights are one
-//    shuffle reduction, and every piece's partial row is loaded before any is used, so a
-//    row costs about one memory round trip.  Eight rows per CTA at a time.
+//    shuffle reduction.  Each warp takes a contiguous run of rows (consecutive rows share
+//    their unit, so the unit's entry is read once), and the next row's log2-sum-exps and
+//    partial rows are in flight while the current row is merged: a warp's run costs about
+//    one memory round trip plus the arithmetic of its rows.
 //  * Many pieces: one CTA per (unit, row): warp w folds pieces w, w + 8, ... into a running
 //    (max, weight sum, weighted sum), loading the partials of four pieces at a time; the
 //    eight warps' results are then combined in shared memory, so a unit cut into many pieces
 //    is merged by many SMs at once.
-// Every sum runs in a fixed order.
+// Every sum runs in piece order.
+template <int D>
+struct RowBuf {
+  static constexpr int D4 = D / 4;
+  static constexpr int NV = (D4 + 31) / 32;  // float4 columns per lane
+  static constexpr int CH = NV > 1 ? 2 : 4;  // pieces held at once (two rows' worth in flight)
+  float ls;                                  // lane s: piece s's log2-sum-exp
+  float4 o4[CH][NV];
+};
+
+// One row of a few-piece unit: the pieces' log2-sum-exps and the partial rows of the first
+// CH pieces, issued together.  Rows past the unit's query rows load nothing.
+template <int D>
+__device__ __forceinline__ void load_row(const ReduceParams& p, int u, int2 info, int r,
+                                         int lane, RowBuf<D>& b, int s0) {
+  using B = RowBuf<D>;
+  const int rg = (u % p.RB) * p.MP + r;
+  const bool live = rg < p.M;
+  const int ns = info.y;
+  if (s0 == 0)
+    b.ls = (live && lane < ns) ? __ldcg(&p.lse_part[(size_t)piece_slot(info.x, lane) * p.MP + r])
+                               : -INFINITY;
+#pragma unroll
+  for (int j = 0; j < B::CH; ++j) {
+    const int s = s0 + j;
+    const bool ok = live && s < ns;
+    const size_t part = ok ? (size_t)piece_slot(info.x, s) * p.MP + r : 0;
+#pragma unroll
+    for (int v = 0; v < B::NV; ++v) {
+      const int c = lane + 32 * v;
+      b.o4[j][v] = (ok && c < B::D4)
+                       ? __ldcg(reinterpret_cast<const float4*>(p.o_part + part * D) + c)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// Merge the row whose first pieces sit in b and store it.
 template <int D, int QK>
-__device__ __forceinline__ void reduce_row_warp(const ReduceParams& p, int u, int2 info, int r,
-                                                int lane) {
-  constexpr int D4 = D / 4;
-  constexpr int NV = (D4 + 31) / 32;  // float4 columns per lane
-  constexpr int CH = 8;               // pieces loaded at once
-  const int rb = u % p.RB, rg = rb * p.MP + r;
+__device__ __forceinline__ void merge_row(const ReduceParams& p, int u, int2 info, int r,
+                                          int lane, RowBuf<D>& b) {
+  using B = RowBuf<D>;
+  const int rg = (u % p.RB) * p.MP + r;
   if (rg >= p.M) return;  // uniform over the warp
   const int ns = info.y;  // <= kReduceWarpPieces
-  float4 o4[CH][NV];
-  auto load_chunk = [&](int s0) {
-#pragma unroll
-    for (int j = 0; j < CH; ++j) {
-      const int s = s0 + j;
-      const size_t part = s < ns ? (size_t)piece_slot(info.x, s) * p.MP + r : 0;
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const int c = lane + 32 * v;
-        o4[j][v] = (s < ns && c < D4) ? reinterpret_cast<const float4*>(p.o_part + part * D)[c]
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-  };
-  // the row's log2-sum-exps and its first pieces' partial rows are all in flight together
-  const float ls = lane < ns ? p.lse_part[(size_t)piece_slot(info.x, lane) * p.MP + r] : -INFINITY;
-  load_chunk(0);
-  float m = ls;
+  float m = b.ls;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-  const float wl = (ls == -INFINITY) ? 0.f : fast_exp2(ls - m);
+  const float wl = (b.ls == -INFINITY) ? 0.f : fast_exp2(b.ls - m);
   float W = wl;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(kFull, W, o);
-  float4 acc[NV];
+  float4 acc[B::NV];
 #pragma unroll
-  for (int v = 0; v < NV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += CH) {
-    if (s0 > 0) load_chunk(s0);
+  for (int v = 0; v < B::NV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < ns; s0 += B::CH) {
+    if (s0 > 0) load_row<D>(p, u, info, r, lane, b, s0);
 #pragma unroll
-    for (int j = 0; j < CH; ++j) {
+    for (int j = 0; j < B::CH; ++j) {
       const float x = __shfl_sync(kFull, wl, (s0 + j) & 31);  // 0 for pieces past ns
       const float xw = s0 + j < ns ? x : 0.f;
 #pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        acc[v].x += xw * o4[j][v].x;
-        acc[v].y += xw * o4[j][v].y;
-        acc[v].z += xw * o4[j][v].z;
-        acc[v].w += xw * o4[j][v].w;
+      for (int v = 0; v < B::NV; ++v) {
+        acc[v].x += xw * b.o4[j][v].x;
+        acc[v].y += xw * b.o4[j][v].y;
+        acc[v].z += xw * b.o4[j][v].z;
+        acc[v].w += xw * b.o4[j][v].w;
       }
     }
   }
-  const int b = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv;
-  const size_t row = ((size_t)b * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
+  const int bq = u / (p.Hkv * p.RB), g = (u / p.RB) % p.Hkv;
+  const size_t row = ((size_t)bq * p.Sq + rg / p.G) * p.Hq + g * p.G + rg % p.G;
   const float inv = W > 0.f ? 1.f / W : 0.f;
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
+  for (int v = 0; v < B::NV; ++v) {
     const int c = lane + 32 * v;
-    if (c < D4)
+    if (c < B::D4)
       store_out4<QK>(p.out, row * D + 4 * c,
                      make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv));
   }
@@ -222,30 +244,63 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
   // partials, which the decode writes, after it.
   const int nred = __ldcg(&p.hdr[HDR_NRED]), nsmall = __ldcg(&p.hdr[HDR_NRED_SMALL]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ws0 = blockIdx.x * kReduceWarps + warp, wl0 = blockIdx.x;
+  // few-piece rows: warp gw takes rows [w0, w1) of the nsmall * MP
+  const int rows = nsmall * p.R, nw = gridDim.x * kReduceWarps;
+  const int per = (rows + nw - 1) / nw, gw = blockIdx.x * kReduceWarps + warp;
+  const int w0 = min(gw * per, rows), w1 = min(w0 + per, rows);
+  const int wl0 = blockIdx.x;
   int us0 = 0, ul0 = 0;
   int2 infos0 = make_int2(0, 0), infol0 = make_int2(0, 0);
-  if (ws0 < nsmall * p.MP) {
-    us0 = __ldcg(&p.red_units[ws0 / p.MP]);
+  if (w0 < w1) {
+    us0 = __ldcg(&p.red_units[w0 / p.R]);
     infos0 = __ldcg(&p.unit_info[us0]);
   }
-  if (wl0 < (nred - nsmall) * p.MP) {
-    ul0 = __ldcg(&p.red_units[nsmall + wl0 / p.MP]);
+  if (wl0 < (nred - nsmall) * p.R) {
+    ul0 = __ldcg(&p.red_units[nsmall + wl0 / p.R]);
     infol0 = __ldcg(&p.unit_info[ul0]);
   }
   grid_dependency_wait();  // partials come from the decode kernel launched just before
   // the next kernel may start launching now: it is held in its own grid_dependency_wait
   // until this grid has completed, and it cannot take the place of a CTA of this grid
   grid_dependents_launch();
-  // few-piece units: a warp per row
-  for (int w = ws0; w < nsmall * p.MP; w += gridDim.x * kReduceWarps) {
-    const int u = w == ws0 ? us0 : __ldcg(&p.red_units[w / p.MP]);
-    const int2 info = w == ws0 ? infos0 : __ldcg(&p.unit_info[u]);
-    reduce_row_warp<D, QK>(p, u, info, w % p.MP, lane);
+  // few-piece units: the next row's loads are issued before the current row is merged
+  if (w0 < w1) {
+    RowBuf<D> ba, bb;
+    int u = us0;
+    int2 info = infos0;
+    load_row<D>(p, u, info, w0 % p.R, lane, ba, 0);
+    // the row after w (its unit's entry read again only where the unit changes)
+    auto next_meta = [&](int w, int& un, int2& in) {
+      un = u;
+      in = info;
+      if ((w + 1) % p.R == 0) {
+        un = __ldcg(&p.red_units[(w + 1) / p.R]);
+        in = __ldcg(&p.unit_info[un]);
+      }
+    };
+    for (int w = w0; w < w1; w += 2) {
+      int un = u;
+      int2 in = info;
+      if (w + 1 < w1) {
+        next_meta(w, un, in);
+        load_row<D>(p, un, in, (w + 1) % p.R, lane, bb, 0);
+      }
+      merge_row<D, QK>(p, u, info, w % p.R, lane, ba);
+      if (w + 1 >= w1) break;
+      u = un;
+      info = in;
+      if (w + 2 < w1) {
+        next_meta(w + 1, un, in);
+        load_row<D>(p, un, in, (w + 2) % p.R, lane, ba, 0);
+      }
+      merge_row<D, QK>(p, u, info, (w + 1) % p.R, lane, bb);
+      u = un;
+      info = in;
+    }
   }
   // many-piece units: a CTA per row
-  for (int w = wl0; w < (nred - nsmall) * p.MP; w += gridDim.x) {
-    const int u = w == wl0 ? ul0 : __ldcg(&p.red_units[nsmall + w / p.MP]), r = w % p.MP;
+  for (int w = wl0; w < (nred - nsmall) * p.R; w += gridDim.x) {
+    const int u = w == wl0 ? ul0 : __ldcg(&p.red_units[nsmall + w / p.R]), r = w % p.R;
     const int rb = u % p.RB, rg = rb * p.MP + r;
     if (rg >= p.M) continue;  // uniform over the CTA
     const int2 info = w == wl0 ? infol0 : __ldcg(&p.unit_info[u]);
@@ -345,8 +400,33 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
   }
 }
 
+// CTAs of a reduce kernel instance that fit on one SM at once, per device (0: not yet asked).
+template <int D, int QK>
+int reduce_blocks_per_sm() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, reduce_kernel<D, QK>, kReduceWarps * 32, 0) !=
+      cudaSuccess)
+    return 0;
+  if (dev >= 0 && dev < 64 && nb > 0) cached[dev].store(nb, std::memory_order_relaxed);
+  return nb;
+}
+
+// need: CTAs the rows could use; the grid is capped at what fits on the GPU at once, so every
+// CTA is resident when the decode has finished and the warps' runs of rows overlap their loads
 template <int D>
-cudaError_t launch_reduce_d(const ReduceParams& p, int q_kind, int grid, cudaStream_t s) {
+cudaError_t launch_reduce_d(const ReduceParams& p, int q_kind, long long need, int sms,
+                            cudaStream_t s) {
+  const int per_sm = q_kind == Q_BF16 ? reduce_blocks_per_sm<D, Q_BF16>()
+                                      : reduce_blocks_per_sm<D, Q_FP16>();
+  if (per_sm <= 0) return cudaErrorUnknown;
+  const int grid = (int)std::max(1LL, std::min(need, (long long)per_sm * sms));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kReduceWarps * 32);
@@ -378,11 +458,13 @@ cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s) {
   p.M = a.v.rows;
   p.RB = a.v.rb;
   p.MP = a.v.mp;
+  p.R = a.v.rb == 1 ? std::min(a.v.rows, a.v.mp) : a.v.mp;
   if (a.v.units == 0) return cudaSuccess;
-  // Rows to merge: few-piece units take a warp per (unit, row), so at most units x mp / 8
-  // CTAs; many-piece units a CTA per row, and as a unit of more than kReduceWarpPieces
-  // pieces holds that many of the 2C partial slots, at most 2C / (kReduceWarpPieces + 1)
-  // units are of that kind.  Eight CTAs per SM at most; the CTAs loop past that.
+  // Rows to merge (R a unit): few-piece units take a warp per (unit, row), so at most
+  // units x R / 8 CTAs; many-piece units a CTA per row, and as a unit of more than
+  // kReduceWarpPieces pieces holds that many of the 2C partial slots, at most
+  // 2C / (kReduceWarpPieces + 1) units are of that kind.  The grid is capped at the CTAs that
+  // fit at once; each warp then takes a run of rows, each CTA every grid-th many-piece row.
   int sms = a.v.sms;
   if (sms <= 0) {
     int dev = 0;
@@ -390,16 +472,15 @@ cudaError_t launch_reduce(const DecodeArgs& a, cudaStream_t s) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return cudaErrorUnknown;
   }
-  const long long units = a.v.units, mp = a.v.mp;
+  const long long units = a.v.units, rows = p.R;
   const long long large_units =
       std::min(units, 2LL * a.v.ctas / (kReduceWarpPieces + 1));
-  const long long need = std::max((units * mp + kReduceWarps - 1) / kReduceWarps,
-                                  large_units * mp);
-  const int grid = (int)std::max(1LL, std::min(need, 8LL * sms));
+  const long long need = std::max((units * rows + kReduceWarps - 1) / kReduceWarps,
+                                  large_units * rows);
   switch (a.p.head_dim) {
-    case 64: return launch_reduce_d<64>(p, a.q_kind, grid, s);
-    case 128: return launch_reduce_d<128>(p, a.q_kind, grid, s);
-    case 256: return launch_reduce_d<256>(p, a.q_kind, grid, s);
+    case 64: return launch_reduce_d<64>(p, a.q_kind, need, sms, s);
+    case 128: return launch_reduce_d<128>(p, a.q_kind, need, sms, s);
+    case 256: return launch_reduce_d<256>(p, a.q_kind, need, sms, s);
     default: return cudaErrorNotSupported;
   }
 }
