@@ -145,9 +145,9 @@ constexpr int kReduceWarps = 8;
 //    partial rows are in flight while the current row is merged: a warp's run costs about
 //    one memory round trip plus the arithmetic of its rows.
 //  * Many pieces: one CTA per (unit, row): warp w folds pieces w, w + 8, ... into a running
-//    (max, weight sum, weighted sum), loading the partials of four pieces at a time; the
-//    eight warps' results are then combined in shared memory, so a unit cut into many pieces
-//    is merged by many SMs at once.
+//    (max, weight sum, weighted sum), loading the partials of four pieces at a time (the
+//    first four with the log2-sum-exps); the eight warps' results are then combined in
+//    shared memory, so a unit cut into many pieces is merged by many SMs at once.
 // Every sum runs in piece order.
 template <int D>
 struct RowBuf {
@@ -308,14 +308,31 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
     float4 acc[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // batches of up to 32 pieces per warp: lane j holds the weight of piece s0 + 8 j
+    // batches of up to 32 pieces per warp: lane j holds the weight of piece s0 + 8 j; the
+    // batch's log2-sum-exps and its first four partial rows are loaded together
     for (int s0 = warp; s0 < info.y; s0 += 32 * kReduceWarps) {
       const int sl = s0 + lane * kReduceWarps;
+      const int cnt = min(32, (info.y - s0 + kReduceWarps - 1) / kReduceWarps);
+      float4 o[4][NV];
+      auto load4 = [&](int j0) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const bool ok = j0 + jj < cnt;
+          const size_t part = ok ? (size_t)piece_slot(info.x, s0 + (j0 + jj) * kReduceWarps) * p.MP + r : 0;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            const int c = lane + 32 * v;
+            o[jj][v] = (ok && c < D4) ? reinterpret_cast<const float4*>(p.o_part + part * D)[c]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      };
       const float ls = sl < info.y ? p.lse_part[(size_t)piece_slot(info.x, sl) * p.MP + r]
                                    : -INFINITY;
+      load4(0);
       float mb = ls;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+      for (int o2 = 16; o2 > 0; o2 >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o2));
       if (mb == -INFINITY) continue;  // no key of this row in the batch (uniform)
       const float mn = fmaxf(m, mb);
       const float sc = m == -INFINITY ? 0.f : fast_exp2(m - mn);
@@ -331,33 +348,20 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_kernel(const ReduceP
       const float wl = ls == -INFINITY ? 0.f : fast_exp2(ls - m);
       float wsum = wl;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(kFull, wsum, o);
+      for (int o2 = 16; o2 > 0; o2 >>= 1) wsum += __shfl_xor_sync(kFull, wsum, o2);
       W += wsum;
-      const int cnt = min(32, (info.y - s0 + kReduceWarps - 1) / kReduceWarps);
       for (int j0 = 0; j0 < cnt; j0 += 4) {
-        float wj[4];
-        float4 o[4][NV];
+        if (j0 > 0) load4(j0);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          wj[jj] = __shfl_sync(kFull, wl, (j0 + jj) & 31);
-          const bool ok = j0 + jj < cnt;
-          const size_t part = ok ? (size_t)piece_slot(info.x, s0 + (j0 + jj) * kReduceWarps) * p.MP + r : 0;
+          const float x = __shfl_sync(kFull, wl, (j0 + jj) & 31);
+          const float xw = j0 + jj < cnt ? x : 0.f;
 #pragma unroll
           for (int v = 0; v < NV; ++v) {
-            const int c = lane + 32 * v;
-            o[jj][v] = (ok && c < D4) ? reinterpret_cast<const float4*>(p.o_part + part * D)[c]
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const float x = j0 + jj < cnt ? wj[jj] : 0.f;
-#pragma unroll
-          for (int v = 0; v < NV; ++v) {
-            acc[v].x += x * o[jj][v].x;
-            acc[v].y += x * o[jj][v].y;
-            acc[v].z += x * o[jj][v].z;
-            acc[v].w += x * o[jj][v].w;
+            acc[v].x += xw * o[jj][v].x;
+            acc[v].y += xw * o[jj][v].y;
+            acc[v].z += xw * o[jj][v].z;
+            acc[v].w += xw * o[jj][v].w;
           }
         }
       }
