@@ -853,6 +853,13 @@ __global__ void __launch_bounds__(TcTraits<D_, MP, KVK, TOKS>::NTHREADS, 1)
       umma_commit(mma_end);
       if (!mbar_wait_drain(mma_end, 0)) atomicOr(s_flags, PA_FLAG_WAIT_TIMEOUT);
     }
+    // 16-bit caches: the idle lanes wait here for lane 0.  The divergent paths of a warp run
+    // one after the other, and lanes 1-31 going on to the final wait on the grid before (the
+    // previous decode, when launched back to back) held lane 0's MMAs until it had ended
+    // (back-to-back decodes of head dim 256, Sq = 64: 174.7 -> 164.5 us at B = 8).  With an
+    // fp8 cache the same convergence point measured slower (74.7 -> 77.3 us), so there the
+    // lanes go on.
+    if constexpr (!T::FP8) __syncwarp();
   } else if (warp < T::W_CONV) {
     // ================================================================ softmax and epilogue
     constexpr bool DUAL = T::DUAL;
